@@ -1,0 +1,305 @@
+"""Seeded synthetic inputs for the multi-LoRA linear layer (shared by the oracle and the CUDA path).
+
+This module draws random numbers and lays out the workloads; it contains none of
+the layer's arithmetic (no scaling factor, no product, no sort). Everything is
+keyed by (seed, tensor id, element index) through the counter-based generator in
+``philox_normal.c``, so any slice of any tensor can be regenerated alone.
+
+The workload recipes follow the shapes and distributions that the pages give:
+- "Multi-LoRA Serving Explained" (sevydevy.com), sections on the weight-matrix
+  maths and the stacked slot pool: hidden 4096, MLP 14336, ranks 8/16/64.
+- "[RFC] Per-request activation of multiple LoRA adapters" (vLLM issue 51940),
+  "Proposed Change": k adapters per request, per-adapter scales, sentinel fill.
+- "[vLLM] LoRA" (secrett2633 blog), PEFTHelper: rsLoRA flag per adapter.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "philox_normal.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libsynth.so")
+_lib = None
+_lock = threading.Lock()
+
+SEED_BASE = 0x6D4C6F52
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator with gcc (host code only, no -march, no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u64, i32, dbl, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+            lib.synth_philox4x64_10.argtypes = [vp, vp, vp]
+            lib.synth_normal_bf16.argtypes = [u64, u64, u64, u64, dbl, vp, i32]
+            lib.synth_normal_f64.argtypes = [u64, u64, u64, u64, dbl, vp, i32]
+            lib.synth_u64.argtypes = [u64, u64, u64, u64, vp, i32]
+            _lib = lib
+    return _lib
+
+
+def _threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def philox4x64_10(counter, key) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
+    out = np.zeros(4, dtype=np.uint64)
+    _load().synth_philox4x64_10(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    return out
+
+
+def tensor_key(*parts: int) -> int:
+    """Pack small non-negative ints (each < 2^12, at most 5) into one 64-bit tensor id."""
+    key = 0
+    assert len(parts) <= 5
+    for p in parts:
+        assert 0 <= p < (1 << 12), p
+        key = (key << 12) | int(p)
+    return key | (len(parts) << 60)
+
+
+def normal_bf16(seed: int, tid: int, shape, std: float = 1.0, first: int = 0) -> np.ndarray:
+    """bf16 bit patterns (uint16) of std * N(0,1), elements [first, first + prod(shape))."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    if n:
+        _load().synth_normal_bf16(seed, tid, first, n, float(std), out.ctypes.data, _threads())
+    return out.reshape(shape)
+
+
+def normal_f64(seed: int, tid: int, shape, std: float = 1.0, first: int = 0) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float64)
+    if n:
+        _load().synth_normal_f64(seed, tid, first, n, float(std), out.ctypes.data, _threads())
+    return out.reshape(shape)
+
+
+def raw_u64(seed: int, tid: int, n: int, first: int = 0) -> np.ndarray:
+    out = np.empty(int(n), dtype=np.uint64)
+    if n:
+        _load().synth_u64(seed, tid, first, int(n), out.ctypes.data, _threads())
+    return out
+
+
+def uniform01(seed: int, tid: int, n: int) -> np.ndarray:
+    """Uniform [0, 1) doubles from the top 53 bits of each word."""
+    return (raw_u64(seed, tid, n) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# --------------------------------------------------------------------------------------
+# Workload recipes
+# --------------------------------------------------------------------------------------
+
+# tensor-id namespaces (first packed field)
+_NS_W, _NS_X, _NS_A, _NS_B, _NS_SLOTS, _NS_SCALES, _NS_MISC = 1, 2, 3, 4, 5, 6, 7
+
+
+@dataclass
+class Adapter:
+    """One LoRA adapter for one linear: A [rank, K], B [D, rank] as bf16 bits."""
+    A: np.ndarray
+    B: np.ndarray
+    rank: int
+    alpha: float
+    rslora: bool = False
+
+
+@dataclass
+class Linear:
+    name: str
+    K: int
+    D: int
+    W: np.ndarray | None            # [D, K] bf16 bits (None when generated lazily by rows)
+    x_id: int                       # which activation matrix feeds it
+    adapters: dict = field(default_factory=dict)   # slot -> Adapter
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    T: int
+    J: int
+    n_slots: int
+    r_max: int
+    token_slots: np.ndarray         # [T, J] int32, -1 = no adapter
+    scales: np.ndarray | None       # [T, J] float32 or None (= 1)
+    xs: dict                        # x_id -> [T, K] bf16 bits
+    linears: list
+    notes: str = ""
+
+
+def _adapter(seed, layer, module, adapter_id, K, D, rank, alpha, rslora, std=0.02):
+    A = normal_bf16(seed, tensor_key(_NS_A, layer, module, adapter_id), (rank, K), std)
+    B = normal_bf16(seed, tensor_key(_NS_B, layer, module, adapter_id), (D, rank), std)
+    return Adapter(A=A, B=B, rank=rank, alpha=float(alpha), rslora=bool(rslora))
+
+
+def tiny(T: int = 16, K: int = 256, D: int = 256, n_adapters: int = 4, rank: int = 8,
+         alpha: float = 16.0, seed_offset: int = 1) -> Workload:
+    """One linear d=k=256, bf16 W ~ N(0, 0.02); 4 adapters of rank 8 (A, B ~ N(0, 0.02), alpha 16);
+    16 tokens of x ~ N(0, 1); per-token slot uniform over {-1, 0, 1, 2, 3}; k = 1, s = 1."""
+    seed = SEED_BASE + seed_offset
+    slots = (raw_u64(seed, tensor_key(_NS_SLOTS), T) % np.uint64(n_adapters + 1)).astype(np.int64) - 1
+    lin = Linear("linear", K, D, normal_bf16(seed, tensor_key(_NS_W, 0, 0), (D, K), 0.02), 0)
+    for s in range(n_adapters):
+        lin.adapters[s] = _adapter(seed, 0, 0, s, K, D, rank, alpha, False)
+    return Workload("tiny", seed, T, 1, n_adapters, rank,
+                    slots.astype(np.int32).reshape(T, 1), None,
+                    {0: normal_bf16(seed, tensor_key(_NS_X, 0), (T, K), 1.0)}, [lin])
+
+
+def decode(T: int = 256, hidden: int = 4096, n_adapters: int = 100, rank: int = 16,
+           alpha: float = 32.0, p_sentinel: float = 0.1, modules=("q", "k", "v", "o"),
+           seed_offset: int = 2) -> Workload:
+    """Decode batch: T tokens at hidden 4096 through q/k/v/o-shaped 4096->4096 linears; 100 resident
+    adapters of rank 16 (alpha 32) per linear; per-token slot uniform over the 100, with a 10 %
+    chance of the sentinel -1. q, k and v read the same x, o reads a second one."""
+    seed = SEED_BASE + seed_offset
+    u = uniform01(seed, tensor_key(_NS_SLOTS, 0), T)
+    pick = (raw_u64(seed, tensor_key(_NS_SLOTS, 1), T) % np.uint64(n_adapters)).astype(np.int64)
+    slots = np.where(u < p_sentinel, -1, pick).astype(np.int32).reshape(T, 1)
+    linears = []
+    for m, name in enumerate(modules):
+        lin = Linear(name, hidden, hidden,
+                     normal_bf16(seed, tensor_key(_NS_W, 0, m), (hidden, hidden), 0.02),
+                     1 if name == "o" else 0)
+        for s in range(n_adapters):
+            lin.adapters[s] = _adapter(seed, 0, m, s, hidden, hidden, rank, alpha, False)
+        linears.append(lin)
+    xs = {0: normal_bf16(seed, tensor_key(_NS_X, 0), (T, hidden), 1.0)}
+    if any(l.x_id == 1 for l in linears):
+        xs[1] = normal_bf16(seed, tensor_key(_NS_X, 1), (T, hidden), 1.0)
+    return Workload("decode", seed, T, 1, n_adapters, rank, slots, None, xs, linears)
+
+
+def prefill(n_requests: int = 8, seg_len: int = 512, hidden: int = 4096, mlp: int = 14336,
+            ranks=(8, 16, 64), r_max: int = 64, seed_offset: int = 3, lazy_w: bool = False) -> Workload:
+    """Prefill batch: 8 requests of 512 contiguous tokens, request i on slot i; fused gate_up
+    4096 -> 2*14336 and down 14336 -> 4096; ranks cycle 8/16/64 padded to r_max 64; alpha = 2r."""
+    seed = SEED_BASE + seed_offset
+    T = n_requests * seg_len
+    slots = np.repeat(np.arange(n_requests, dtype=np.int32), seg_len).reshape(T, 1)
+    shapes = [("gate_up", hidden, 2 * mlp, 0), ("down", mlp, hidden, 1)]
+    linears = []
+    for m, (name, K, D, xid) in enumerate(shapes):
+        W = None if lazy_w else normal_bf16(seed, tensor_key(_NS_W, 0, m), (D, K), 0.02)
+        lin = Linear(name, K, D, W, xid)
+        for s in range(n_requests):
+            r = ranks[s % len(ranks)]
+            lin.adapters[s] = _adapter(seed, 0, m, s, K, D, r, 2.0 * r, False)
+        linears.append(lin)
+    xs = {0: normal_bf16(seed, tensor_key(_NS_X, 0), (T, hidden), 1.0),
+          1: normal_bf16(seed, tensor_key(_NS_X, 1), (T, mlp), 1.0)}
+    return Workload("prefill", seed, T, 1, n_requests, r_max, slots, None, xs, linears)
+
+
+def compose(T: int = 128, hidden: int = 4096, qkv_out: int = 6144, n_adapters: int = 32,
+            rank: int = 16, alpha: float = 32.0, J: int = 3, seed_offset: int = 4) -> Workload:
+    """Multi-adapter decode: T tokens, qkv 4096 -> 6144; each token draws n ~ U{1..J} adapters
+    without replacement from 32 rank-16 adapters, trailing slots -1; per-request scales
+    U[0.2, 1.0] (fp32); adapters with an even slot id use rsLoRA."""
+    seed = SEED_BASE + seed_offset
+    n_act = (raw_u64(seed, tensor_key(_NS_SLOTS, 0), T) % np.uint64(J)).astype(np.int64) + 1
+    words = raw_u64(seed, tensor_key(_NS_SLOTS, 1), T * J).reshape(T, J)
+    slots = np.full((T, J), -1, dtype=np.int32)
+    for t in range(T):
+        pool = list(range(n_adapters))
+        for j in range(int(n_act[t])):          # partial Fisher-Yates, without replacement
+            i = j + int(words[t, j] % np.uint64(n_adapters - j))
+            pool[j], pool[i] = pool[i], pool[j]
+            slots[t, j] = pool[j]
+    u = uniform01(seed, tensor_key(_NS_SCALES, 0), T * J).reshape(T, J)
+    scales = (0.2 + 0.8 * u).astype(np.float32)
+    scales[slots < 0] = 0.0
+    lin = Linear("qkv", hidden, qkv_out,
+                 normal_bf16(seed, tensor_key(_NS_W, 0, 0), (qkv_out, hidden), 0.02), 0)
+    for s in range(n_adapters):
+        lin.adapters[s] = _adapter(seed, 0, 0, s, hidden, qkv_out, rank, alpha, s % 2 == 0)
+    xs = {0: normal_bf16(seed, tensor_key(_NS_X, 0), (T, hidden), 1.0)}
+    return Workload("compose", seed, T, J, n_adapters, rank, slots, scales, xs, [lin])
+
+
+def zipf_admission(n_requests: int, n_ids: int, exponent: float, max_distinct: int,
+                   seed: int, tid: int) -> list:
+    """Draw request tenants from Zipf(exponent) over ids 1..n_ids and admit them in order: a
+    request whose adapter is new is deferred when the batch already holds max_distinct adapters
+    (the max-loras admission rule). Returns the admitted tenant ids in admission order."""
+    w = 1.0 / np.arange(1, n_ids + 1, dtype=np.float64) ** exponent
+    cdf = np.cumsum(w) / w.sum()
+    admitted, distinct, i = [], [], 0
+    u = uniform01(seed, tid, 64 * n_requests + 64)
+    while len(admitted) < n_requests and i < len(u):
+        a = int(np.searchsorted(cdf, u[i], side="right")) + 1
+        i += 1
+        if a not in distinct:
+            if len(distinct) >= max_distinct:
+                continue
+            distinct.append(a)
+        admitted.append(a)
+    return admitted
+
+
+def mixed_step_plan(n_prefill: int = 4, prefill_len: int = 192, n_decode: int = 256,
+                    n_registered: int = 1000, n_slots: int = 128, zipf: float = 1.1,
+                    seed_offset: int = 5):
+    """Mixed serving step: 4 prefill segments of 192 tokens (one request each) then 256 decode
+    tokens (one request each); tenants Zipf(1.1) over 1000 registered ids; admitted adapters
+    map to slots 0..n-1 in first-seen order; rank by id is [8, 16, 64][id mod 3], alpha = 2r."""
+    seed = SEED_BASE + seed_offset
+    tenants = zipf_admission(n_prefill + n_decode, n_registered, zipf, n_slots, seed,
+                             tensor_key(_NS_MISC, 0))
+    slot_of = {}
+    for a in tenants:
+        slot_of.setdefault(a, len(slot_of))
+    per_token = []
+    for i, a in enumerate(tenants):
+        per_token += [slot_of[a]] * (prefill_len if i < n_prefill else 1)
+    T = len(per_token)
+    ranks = {a: (8, 16, 64)[a % 3] for a in slot_of}
+    return dict(seed=seed, T=T, token_slots=np.array(per_token, dtype=np.int32).reshape(T, 1),
+                slot_of=slot_of, rank_of=ranks, tenants=tenants)
+
+
+MIXED_MODULES = (("qkv", 4096, 6144, 0), ("o", 4096, 4096, 1),
+                 ("gate_up", 4096, 28672, 2), ("down", 14336, 4096, 3))
+
+
+def mixed_adapter(seed: int, layer: int, module: int, adapter_id: int, K: int, D: int) -> Adapter:
+    r = (8, 16, 64)[adapter_id % 3]
+    return _adapter(seed, layer, module, adapter_id, K, D, r, 2.0 * r, False)
+
+
+def mixed_weight_rows(seed: int, layer: int, module: int, K: int, row0: int, n_rows: int) -> np.ndarray:
+    return normal_bf16(seed, tensor_key(_NS_W, layer, module), (n_rows, K), 0.02, first=row0 * K)
+
+
+def mixed_x(seed: int, layer: int, module: int, T: int, K: int) -> np.ndarray:
+    return normal_bf16(seed, tensor_key(_NS_X, layer, module), (T, K), 1.0)
