@@ -1,0 +1,416 @@
+"""Benchmark of the multi-LoRA batched linear layer on GB300.
+
+Workload (default): the decode batch of the pages' shapes -- 256 tokens at hidden 4096
+through four q/k/v/o-shaped 4096 -> 4096 bf16 linears, each with its own pool of 100
+resident rank-16 adapters (alpha 32); per-token slot uniform over the 100 with 10 % of
+tokens on the sentinel -1. One step = build the slot metadata once, then the four
+linears (base GEMM + shrink + expand each). Metric: tokens per second through the step.
+
+Output: one JSON line (rank 0). Kernel durations for the roofline come from a second
+pass of the same K steps with per-kernel CUDA events (the library's trace), so that the
+events do not slow the headline timing. L2 is flushed (256 MiB write) before every timed
+step, outside the timed events.
+
+--impl reference times the fp64 CPU oracle (the only reference this subject has) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-linear tokens/s (1×GB300) + % of HBM / bf16 tensor roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------ workload
+def make_workload(name: str):
+    import synth
+    if name == "decode":
+        return synth.decode()
+    if name == "compose":
+        return synth.compose()
+    if name == "tiny":
+        return synth.tiny()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def workload_config(wl, name: str) -> dict:
+    lin = wl.linears
+    return {
+        "workload": f"{name}: T={wl.T} tokens, J={wl.J}, linears "
+                    + ", ".join(f"{l.name} {l.K}->{l.D}" for l in lin)
+                    + f", {wl.n_slots} slots r_max={wl.r_max}",
+        "tokens_per_step": wl.T,
+        "linears": len(lin),
+        "slots": wl.n_slots,
+        "r_max": wl.r_max,
+        "slots_per_token": wl.J,
+        "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+    }
+
+
+def algorithmic_bytes(wl) -> dict:
+    """Bytes each kernel kind must move per step (unique data, counted once):
+    base GEMM: W + x + y write (fp32); shrink: A rows of the distinct active slots (true rank)
+    + x rows of active tokens + v write; expand: B rows of the distinct active slots (true rank,
+    padded to 8) + y read-modify-write of rows with an active slot + v read.
+    Flops: 2*T*K*D per linear for the base product."""
+    slots = wl.token_slots
+    active = slots >= 0
+    act_rows = int(np.any(active, axis=1).sum())
+    pairs = int(active.sum())
+    distinct = sorted(set(int(s) for s in slots[active]))
+    out = {"base_gemm": 0, "shrink": 0, "expand": 0, "base_flops": 0, "meta": 0}
+    for l in wl.linears:
+        out["base_gemm"] += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
+        out["base_flops"] += 2 * wl.T * l.K * l.D
+        ra = sum(l.adapters[s].rank for s in distinct)
+        rb = sum((l.adapters[s].rank + 7) // 8 * 8 for s in distinct)
+        out["shrink"] += ra * l.K * 2 + act_rows * l.K * 2 + pairs * wl.r_max * 4
+        out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * wl.r_max * 4
+    out["meta"] = wl.T * wl.J * 4 * 6
+    return out
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ oracle timing
+def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
+    """Times the fp64 oracle on a bounded sample of the workload: all linears of the step for a
+    growing number of token rows until about budget_s of CPU work. Returns tokens/s, rows, threads."""
+    import oracle
+    threads = oracle.default_threads()
+    T = wl.T
+    cap = T if max_rows is None else min(T, max_rows)
+    rows_n = min(cap, max(1, threads))
+    spent, tokens = 0.0, 0
+    rng = np.random.default_rng(0)
+    while True:
+        rows = np.sort(rng.choice(T, size=rows_n, replace=False))
+        t0 = time.perf_counter()
+        for l in wl.linears:
+            oracle.linear(wl.xs[l.x_id], l.W, wl.token_slots, l.adapters, wl.n_slots, scales=wl.scales,
+                          rows=rows, threads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        tokens = rows_n
+        last = dt
+        if rows_n >= cap or spent + dt * 2.5 > budget_s:
+            break
+        rows_n = min(cap, rows_n * 2)
+    return tokens / last, tokens, threads, last
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = make_workload(args.workload)
+    step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    rows = None
+    times = []
+    for i in range(args.warmup + args.steps):
+        tps, rows, threads, dt = oracle_sample(wl, budget_s=step_budget, max_rows=rows)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * float(np.mean(times))
+    value = rows / (ms / 1000.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
+        "config": workload_config(wl, args.workload),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ our arm
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rank_adapter_gemm_token_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or None when
+    missing or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+    except ValueError:
+        return None
+    r = rec.get(workload, {}).get(kind)
+    if not r or r.get("kernel_hash") != kernel_hash():
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from rank_adapter_gemm_token_gb300 import mlora
+    from tests.harness import DeviceWorkload
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local)) if "device_id" in \
+            dist.init_process_group.__code__.co_varnames else dist.init_process_group("nccl")
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+
+    wl = make_workload(args.workload)
+    dw = DeviceWorkload(wl, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        dw.run(stream)
+    dw.meta.status()
+    barrier()
+
+    # ---- headline: K timed steps, L2 flushed before each, no tracing
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = mlora.mlora_launch_count()
+    barrier()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        dw.run(stream)
+        ends[i].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    launches = mlora.mlora_launch_count() - launches0
+    clock_info = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = float(np.mean(step_ms))
+    if ws > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * wl.T / (ms / 1000.0)
+
+    # ---- per-kernel durations: the same K steps again with the library's event trace
+    mlora.mlora_trace_enable(64 * args.steps + 64)
+    for i in range(args.steps):
+        flush.zero_()
+        dw.run(stream)
+    barrier()
+    trace = mlora.mlora_trace_read()
+    mlora.mlora_trace_disable()
+
+    # ---- end to end: pinned host inputs in, step, result out, every step
+    xs_host = {k: v.cpu().pin_memory() for k, v in dw.x.items()}
+    slots_host = dw.token_slots.cpu().pin_memory()
+    scales_host = None if dw.scales is None else dw.scales.cpu().pin_memory()
+    ys_host = [torch.empty(dl.y.shape, dtype=dl.y.dtype).pin_memory() for dl in dw.linears]
+    h2d = sum(v.numel() * v.element_size() for v in xs_host.values()) + slots_host.numel() * 4 + \
+        (0 if scales_host is None else scales_host.numel() * 4)
+    d2h = sum(y.numel() * y.element_size() for y in ys_host)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.zero_()
+        e_start.record(stream)
+        for k, v in xs_host.items():
+            dw.x[k].copy_(v, non_blocking=True)
+        dw.token_slots.copy_(slots_host, non_blocking=True)
+        if scales_host is not None:
+            dw.scales.copy_(scales_host, non_blocking=True)
+        dw.run(stream)
+        for dl, yh in zip(dw.linears, ys_host):
+            yh.copy_(dl.y, non_blocking=True)
+        e_end.record(stream)
+        e_end.synchronize()
+        e2e_ms.append(e_start.elapsed_time(e_end))
+    e2e_value = ws * wl.T / (float(np.mean(e2e_ms)) / 1000.0)
+    dw.meta.status()
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    algo = algorithmic_bytes(wl)
+    kinds = {k: v for k, v in trace.items() if v[0] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][1])
+    n_launch, tot_ms = kinds[dom]
+    avg_s = tot_ms / n_launch / 1000.0
+    launches_per_step = n_launch / args.steps
+    if dom == "base_gemm":
+        flops = algo["base_flops"] / launches_per_step
+        byts = algo["base_gemm"] / launches_per_step
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if flops / byts > ridge else "hbm"
+    else:
+        byts = algo.get(dom, 0) / launches_per_step
+        flops, bound = 0, "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = flops / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = byts / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
+                if peak_src == "measured" else "fallback",
+                "traffic": recorded_traffic(dom, args.workload),
+                "algorithmic_bytes_per_launch": byts, "avg_launch_us": avg_s * 1e6}
+    per_kernel = {}
+    for k, (n, t) in kinds.items():
+        per = n / args.steps
+        entry = {"launches_per_step": per, "avg_us": 1000.0 * t / n, "share": t / sum(v[1] for v in kinds.values())}
+        if k in algo and algo[k] > 0:
+            entry["achieved_GBps"] = algo[k] / per / (t / n / 1000.0) / 1e9
+            entry["frac_hbm"] = entry["achieved_GBps"] / peaks["hbm_gbs"]
+        if k == "base_gemm":
+            entry["achieved_TFLOPs"] = algo["base_flops"] / per / (t / n / 1000.0) / 1e12
+            entry["frac_bf16"] = entry["achieved_TFLOPs"] / peaks["bf16_tflops"]
+        per_kernel[k] = entry
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        tps, rows, threads, dt = oracle_sample(wl, budget_s=args.cpu_budget)
+        cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears ({dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
+        "config": dict(workload_config(wl, args.workload), parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "clocks": clock_info,
+        "kernels": per_kernel,
+        "wall_s_timed_region": wall,
+        "kernel_timing": "second pass of the same K steps with per-kernel CUDA events on the launch stream",
+    }
+    print(json.dumps(line), flush=True)
+    dw.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "tiny"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,192 @@
+/*
+ * mlora.h -- C ABI of a single-GPU (GB300, sm_103a) multi-LoRA batched linear layer.
+ *
+ * The layer (one adapted linear of a transformer) computes, for a mixed-tenant batch,
+ *
+ *     y[t, :] = x[t, :] W^T  +  sum_{j : slot[t,j] != -1}  s[t,j] * c(slot) * B_slot (A_slot x[t, :])
+ *
+ * with c = alpha / r, or alpha / sqrt(r) for rsLoRA adapters.
+ * Sources:
+ *   "Multi-LoRA Serving Explained" (sevydevy.com): LoRA basics (B is d x r, A is r x k,
+ *     W x + (alpha/r) B(A x)); batched serving (one shared base product plus each token's
+ *     side path, found through a GPU slot number, -1 = base model only); the stacked,
+ *     zero-padded slot pool sized at the maximum rank; rejection of ranks above it.
+ *   "[RFC] Per-request activation of multiple LoRA adapters" (vLLM issue 51940),
+ *     Proposed Change: k adapters per request with per-adapter scales; a k-slot token map
+ *     with unused slots holding the sentinel; a bound on adapters per request.
+ *   "LoRA Serving" (vLLM learning book ch. 09-04), sections 4 and 6: slot activation copies
+ *     an adapter's weights into a GPU slot; the per-step token -> slot mapping; shrink and
+ *     expand.
+ *   "[vLLM] LoRA" (secrett2633 blog), PEFTHelper: r, lora_alpha, use_rslora.
+ *
+ * Conventions
+ *   - bf16 values are passed as their 16-bit patterns (mlora_bf16).
+ *   - "device" pointers are CUDA global-memory pointers of the current device; "host"
+ *     pointers are CPU memory (pinned memory gives asynchronous copies).
+ *   - Streams are cudaStream_t values passed as void*; NULL means the legacy default stream.
+ *   - Every call returns an mlora_status; MLORA_OK is 0. On failure mlora_last_error()
+ *     gives a message for the calling thread. No call throws.
+ *   - Errors of earlier asynchronous work surface as MLORA_ERR_CUDA on a later call.
+ *   - Rows are contiguous (row-major); x rows hold K elements, W rows K, y rows D.
+ *   - K must be a positive multiple of 8; x and W must be 16-byte aligned; y 16-byte aligned.
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLORA_API __attribute__((visibility("default")))
+#else
+#define MLORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mlora_status;
+typedef uint16_t mlora_bf16;
+typedef struct mlora_pool* mlora_pool_t;
+typedef struct mlora_meta* mlora_meta_t;
+
+enum {
+  MLORA_OK = 0,
+  MLORA_ERR_INVALID_ARG = 1,      /* null pointer, bad size, misaligned pointer             */
+  MLORA_ERR_SLOT_RANGE = 2,       /* slot outside [0, n_slots)                              */
+  MLORA_ERR_RANK_TOO_LARGE = 3,   /* adapter rank above the pool's r_max                    */
+  MLORA_ERR_RANK_INVALID = 4,     /* rank < 1, or alpha not finite                           */
+  MLORA_ERR_BAD_TOKEN_SLOT = 5,   /* a token named a slot outside [-1, n_slots) or an empty slot */
+  MLORA_ERR_TOO_MANY_TOKENS = 6,  /* T or J above what the metadata object was created for  */
+  MLORA_ERR_OOM = 7,              /* device or host allocation failed                       */
+  MLORA_ERR_CUDA = 8,             /* a CUDA call failed (message has the CUDA error)         */
+  MLORA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait gave up (the GPU stays usable)  */
+  MLORA_ERR_MISMATCH = 10         /* pool and metadata or pool and operands do not fit     */
+};
+
+/* Limits of this build. */
+#define MLORA_MAX_SLOTS 2048
+#define MLORA_MAX_RANK 256
+#define MLORA_MAX_SLOTS_PER_TOKEN 8
+#define MLORA_MAX_TOKENS 65535
+
+/* ------------------------------------------------------------------ adapter pool ----- */
+
+/* Creates the stacked slot pool of one adapted linear (K inputs, D outputs):
+ *   A_pool [n_slots, R, K] and B_pool [n_slots, D, R] bf16, zero-initialised, where
+ *   R = r_max rounded up to a multiple of 8; a per-slot factor c (fp32) and true rank.
+ * ("Multi-LoRA Serving Explained", max-lora-rank section: slots are zero blocks sized for
+ * the maximum rank; a smaller adapter fills the top-left corner.)
+ * copy_stream: the stream adapter loads run on (NULL: the pool creates its own).
+ * The pool allocates with cudaMalloc here and never on the hot path. */
+MLORA_API mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_stream, mlora_pool_t* out);
+
+/* Waits for this pool's loads and uses to finish, then frees it. NULL is accepted. */
+MLORA_API mlora_status mlora_pool_destroy(mlora_pool_t pool);
+
+/* Copies one adapter into a slot ("LoRA Serving", section 4.1: activating an adapter copies its
+ * weights into a free GPU slot; the caller chooses the slot and keeps the id -> slot map).
+ *   A_host: [rank, K] bf16 row-major, B_host: [D, rank] bf16 row-major (host memory).
+ *   rank <= r_max (else MLORA_ERR_RANK_TOO_LARGE, message naming both ranks), alpha finite.
+ *   rslora != 0 selects c = alpha / sqrt(rank), else c = alpha / rank.
+ * Runs on the pool's copy stream after every mlora_linear already issued on this pool
+ * (write-after-read ordering by event): the slot is zeroed, A is copied to rows 0..rank-1,
+ * B to columns 0..rank-1 (row pitch R). Returns when the copies are queued; with pinned
+ * host buffers they are asynchronous and the buffers must stay valid until
+ * mlora_pool_sync() or the next mlora_linear on this pool has been ordered after them.
+ * With pageable buffers the copy is complete on return. */
+MLORA_API mlora_status mlora_load_adapter(mlora_pool_t pool, int slot, const mlora_bf16* A_host, const mlora_bf16* B_host,
+                                int rank, float alpha, int rslora);
+
+/* Zeroes a slot and marks it empty (tokens naming it are then rejected). */
+MLORA_API mlora_status mlora_clear_slot(mlora_pool_t pool, int slot);
+
+/* Blocks until every queued load of this pool has finished. */
+MLORA_API mlora_status mlora_pool_sync(mlora_pool_t pool);
+
+/* Device pointers and sizes of the pool (for inspection and tests; owned by the pool). */
+MLORA_API mlora_status mlora_pool_info(mlora_pool_t pool, int* n_slots, int* r_pad, int* K, int* D, void** A_pool,
+                             void** B_pool, void** slot_scale, void** slot_rank);
+
+/* Bytes of device memory held by a pool's A and B slots: n_slots * R * (K + D) * 2 with
+ * R = r_max rounded up to 8 ("Multi-LoRA Serving Explained", memory maths: rank * (in + out)
+ * numbers per adapted layer, slots reserved at the maximum rank). 0 for invalid sizes. */
+MLORA_API size_t mlora_pool_bytes(int n_slots, int r_max, int K, int D);
+
+/* ------------------------------------------------------------------ step metadata ---- */
+
+/* Creates a metadata object for steps of at most max_tokens tokens and max_slots_per_token
+ * (J) adapter slots per token ("[RFC] ...", item 5: max_loras_per_request), for pools whose
+ * r_max is at most r_max. Holds the sorted pair order, the segment table, per-pair scales
+ * and the shrink workspace (8 * max_tokens * J * r_max fp32). */
+MLORA_API mlora_status mlora_meta_create(int max_tokens, int max_slots_per_token, int r_max, mlora_meta_t* out);
+MLORA_API mlora_status mlora_meta_destroy(mlora_meta_t meta);
+
+/* Builds one step's metadata on the GPU ("Multi-LoRA Serving Explained", batched serving:
+ * sort the batch's tokens by slot before shrink and expand; "[RFC] ...", item 2: k slots per
+ * token, sentinel -1 in unused ones).
+ *   token_slots: device int32 [T, J]; -1 = no adapter.
+ *   scales:      device fp32 [T, J] per-(token, slot) scale s, or NULL for s = 1.
+ *   pool:        validates slot ids against it (range and loaded); pools used with this
+ *                metadata must have the same n_slots.
+ * Pairs p = t*J + j are stably sorted by slot (-1 first); segments are runs of one slot in
+ * ascending slot order. A pair naming a slot outside [-1, n_slots) or an empty slot is
+ * treated as -1 and recorded; mlora_meta_status() reports it as MLORA_ERR_BAD_TOKEN_SLOT.
+ * Asynchronous on `stream`; T = 0 is allowed. */
+MLORA_API mlora_status mlora_build_meta(mlora_meta_t meta, const int32_t* token_slots, const float* scales, int T, int J,
+                              mlora_pool_t pool, void* stream);
+
+/* Synchronises with the last build/linear that used this metadata and reports device-side
+ * errors (MLORA_ERR_BAD_TOKEN_SLOT with the first rejected pair in the message,
+ * MLORA_ERR_DEVICE_TIMEOUT). Clears the error word. */
+MLORA_API mlora_status mlora_meta_status(mlora_meta_t meta);
+
+/* Copies the metadata to host (synchronising): order [T*J], seg_slot and seg_off
+ * (n_seg and n_seg + 1 entries; arrays sized T*J + 2 suffice), counts. Any pointer may be NULL. */
+MLORA_API mlora_status mlora_meta_read(mlora_meta_t meta, int32_t* order, int32_t* seg_slot, int32_t* seg_off, int* n_seg,
+                             int* n_active);
+
+/* ------------------------------------------------------------------ the layer ------- */
+
+/* y = x W^T + sum_j s c B(A x) for the step described by `meta` ("LoRA Serving", section 7:
+ * y = base_layer(x), then add_lora_linear(y, x, A_stacked, B_stacked, scaling)).
+ *   x: device bf16 [T, K]; W: device bf16 [D, K] (nn.Linear layout); y: device fp32 [T, D],
+ *   overwritten. T is the meta's last build. The base product runs on the tensor cores;
+ *   when the step has no active pair the LoRA kernels do no work, and rows whose slots are
+ *   all -1 equal the base product exactly. Orders itself after the pool's queued loads.
+ * Calls that share a meta or a pool must be ordered on one stream. */
+MLORA_API mlora_status mlora_linear(mlora_pool_t pool, mlora_meta_t meta, const mlora_bf16* x, const mlora_bf16* W, float* y,
+                          void* stream);
+
+/* The same kernels one at a time (for per-kernel tests and timing):
+ *   mlora_base_gemm:   y[T, D] = x[T, K] W[D, K]^T (fp32 out, tcgen05 tensor cores);
+ *   mlora_lora_shrink: v = A_slot x per active pair into the meta's workspace;
+ *   mlora_lora_expand: y += s c B_slot v per active pair (token-major, slot order j). */
+MLORA_API mlora_status mlora_base_gemm(const mlora_bf16* x, const mlora_bf16* W, float* y, int T, int K, int D, void* stream);
+MLORA_API mlora_status mlora_lora_shrink(mlora_pool_t pool, mlora_meta_t meta, const mlora_bf16* x, void* stream);
+MLORA_API mlora_status mlora_lora_expand(mlora_pool_t pool, mlora_meta_t meta, float* y, void* stream);
+
+/* ------------------------------------------------------------------ diagnostics ------ */
+
+MLORA_API const char* mlora_status_string(mlora_status status);
+MLORA_API const char* mlora_last_error(void);      /* thread-local; valid until the thread's next call */
+MLORA_API int mlora_version(void);
+
+/* Kernels this library has launched in this process (all kinds). */
+MLORA_API uint64_t mlora_launch_count(void);
+
+/* Per-kernel CUDA-event trace. While enabled, every kernel launch is bracketed by two events
+ * on its own stream (at most `capacity` launches are kept). mlora_trace_read synchronises
+ * and returns, for each kernel kind, the number of launches and their summed device time in
+ * milliseconds; kinds: 0 meta, 1 base GEMM, 2 shrink, 3 expand, 4 slot bookkeeping. */
+MLORA_API mlora_status mlora_trace_enable(int capacity);
+MLORA_API mlora_status mlora_trace_disable(void);
+MLORA_API mlora_status mlora_trace_read(int n_kinds, int* launches, double* total_ms);
+MLORA_API const char* mlora_kernel_kind_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLORA_H */

@@ -1,0 +1,255 @@
+// Base product of the layer: y[T, D] (fp32) = x[T, K] * W[D, K]^T, bf16 operands.
+//
+// "Multi-LoRA Serving Explained" (sevydevy.com), batched-serving section: every token of
+// the mixed-tenant batch is multiplied by the one shared base weight in a single large
+// matrix product; only the thin side path differs per token. "LoRA Serving" (vLLM
+// learning book, ch. 09-04), section 3: the batch still runs x * W once as one GEMM.
+//
+// sm_103a design: a persistent, warp-specialised kernel on the 5th-generation tensor cores.
+//   warp 0      TMA producer: 128 x 64 tiles of x and BN x 64 tiles of W into a ring of
+//               STAGES shared-memory stages (128-byte swizzle), one mbarrier per stage;
+//   warp 1      allocates 2*BN TMEM columns and issues tcgen05.mma (M=128, N=BN, K=16)
+//               from one thread, committing each stage back to the producer;
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one row per thread) and
+//               stores to y. Two accumulators in TMEM let the epilogue of one tile overlap
+//               the main loop of the next.
+// Tiles are visited M-fastest so that the CTAs working on one W column block run together
+// and W is read from HBM once. Every wait is bounded (2 s): on a timeout the kernel sets
+// an error bit and leaves instead of hanging.
+#include <cuda.h>
+
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mlora {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                    // 64 bf16 = one 128-byte swizzle row
+constexpr int kGemmThreads = 192;
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarrierOffset = STAGES * kStageBytes;
+  static constexpr int kBytes = kBarrierOffset + 256 + 1024;   // + barriers, + alignment slack
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                    float* __restrict__ y, int T, int D, int K, uint32_t* __restrict__ err) {
+  using L = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarrierOffset);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (T + BM - 1) / BM;
+  const int num_n = (D + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 4);       // one arrival per epilogue warp
+    }
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+    ptx::tma_prefetch_desc(&tmap_x);
+    ptx::tma_prefetch_desc(&tmap_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 2 * BN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * BM;
+        const int n0 = (tile / num_m) * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) { ok = false; break; }
+          uint8_t* sa = smem + stage * L::kStageBytes;
+          uint8_t* sb = sa + L::kABytes;
+          ptx::mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
+          ptx::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, m0);
+          ptx::tma_load_2d(sb, &tmap_w, &full[stage], kb * BK, n0);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(&full[stage], phase, err)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(smem + stage * L::kStageBytes);
+          const uint32_t b_addr = a_addr + L::kABytes;
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(a_addr);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(b_addr);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // advancing K by 16 elements = 32 bytes = 2 in the descriptor's address field
+            ptx::umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          ptx::umma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::umma_commit(&acc_full[acc]);
+      }
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int m0 = (tile % num_m) * BM;
+      const int n0 = (tile / num_m) * BN;
+      const int acc = local & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+      if (!ptx::mbar_wait(&acc_full[acc], acc_phase, err)) break;
+      ptx::tc_fence_after();
+      const int row = m0 + row_in_tile;
+      float* yrow = y + static_cast<size_t>(row) * D;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(acc * BN + c);
+        ptx::tmem_ld_32x32b_x32(taddr, r);
+        ptx::tmem_ld_wait();
+        const int col = n0 + c;
+        if (row < T) {
+          if (col + 32 <= D && (D & 3) == 0) {
+            float4* dst = reinterpret_cast<float4*>(yrow + col);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v)
+              if (col + v < D) yrow[col + v] = __uint_as_float(r[v]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] seen as a 2-D tensor, box = box_cols x box_rows, 128B swizzle.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                      int num_sms, cudaStream_t s) {
+  using L = GemmSmem<BN, STAGES>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  CUtensorMap mx, mw;
+  if (!make_tmap_bf16(&mx, x, T, K, BM, BK) || !make_tmap_bf16(&mw, W, D, K, BN, BK))
+    return cudaErrorInvalidValue;
+  const int tiles = ((T + BM - 1) / BM) * ((D + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  note_launch_begin(kKindGemm, s);
+  gemm_bf16_tc_kernel<BN, STAGES><<<grid, kGemmThreads, L::kBytes, s>>>(mx, mw, y, T, D, K, err);
+  cudaError_t e = cudaGetLastError();
+  note_launch_end(kKindGemm, s);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
+                             uint32_t* err, int num_sms, cudaStream_t s) {
+  if (T == 0 || D == 0) return cudaSuccess;
+  // Largest N tile that still gives every SM a tile; small problems take N = 64.
+  const int m_tiles = (T + BM - 1) / BM;
+  if (m_tiles * ((D + 255) / 256) >= num_sms) return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, s);
+  if (m_tiles * ((D + 127) / 128) >= num_sms) return launch_tc<128, 6>(x, W, y, T, K, D, err, num_sms, s);
+  return launch_tc<64, 8>(x, W, y, T, K, D, err, num_sms, s);
+}
+
+}  // namespace mlora

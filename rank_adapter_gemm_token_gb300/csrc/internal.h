@@ -1,0 +1,63 @@
+// Declarations shared by the library's translation units (host launchers and the
+// device-side views of the pool and the per-step metadata). Not part of the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mlora {
+
+constexpr int kMaxSlots = 2048;     // pool slots (GPU-resident adapters)
+constexpr int kMaxRank = 256;       // r_max
+constexpr int kMaxJ = 8;            // adapter slots per token
+constexpr int kPairBlock = 16;      // pairs of one slot handled together by the shrink
+constexpr int kShrinkSplits = 8;    // K is cut into at most this many chunks by the shrink
+constexpr int kMetaThreads = 1024;
+
+// Device arrays of one adapter pool (one adapted linear).
+struct PoolView {
+  const uint16_t* A;        // [S, R, K] bf16, slot s row q at A + (s*R + q)*K
+  const uint16_t* B;        // [S, D, R] bf16, slot s row o at B + (s*D + o)*R
+  const float* slot_scale;  // [S] alpha/r or alpha/sqrt(r)
+  const int32_t* slot_rank; // [S] true rank, 0 = empty slot
+  int S, R, K, D;
+};
+
+// Device arrays of one step's metadata (see build_meta_kernel for the contents).
+struct MetaView {
+  int32_t* order;       // [n] pair indices p = t*J + j, stably sorted by slot (-1 first)
+  int32_t* seg_slot;    // [n + 1] slot of each segment, ascending (-1 first if present)
+  int32_t* seg_off;     // [n + 2] segment offsets into order, n_seg + 1 entries
+  int32_t* pair_slot;   // [n] validated slot per pair (-1: sentinel or rejected)
+  float* pair_scale;    // [n] per-pair scale (0 where pair_slot == -1)
+  int32_t* blk_slot;    // [n] pair-blocks of at most kPairBlock pairs of one slot
+  int32_t* blk_start;   // [n]   start of the block inside order
+  int32_t* blk_count;   // [n]   pairs in the block
+  int32_t* counts;      // [4] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none)
+  uint32_t* err;        // device error word (ptx::kErr* bits)
+  float* vpart;         // shrink output: [n_kchunks][n][R] fp32 partial sums over K chunks
+  int n;                // pairs of the current step (T * J)
+  int T, J;
+};
+
+// Kernel kinds for the launch counter and the optional per-kernel event trace.
+enum KernelKind : int { kKindMeta = 0, kKindGemm = 1, kKindShrink = 2, kKindExpand = 3, kKindSlot = 4, kNumKinds = 5 };
+
+// Launch counter + tracing hooks (mlora_runtime.cu).
+void note_launch_begin(int kind, cudaStream_t s);
+void note_launch_end(int kind, cudaStream_t s);
+
+// Launchers. Each returns the cudaError_t of its launch.
+cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
+                              const int32_t* slot_rank, const MetaView& m, cudaStream_t s);
+
+// y[T, D] (fp32) = x[T, K] (bf16, row-major) * W[D, K]^T (bf16, row-major), tcgen05 path.
+cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
+                             uint32_t* err, int num_sms, cudaStream_t s);
+
+int shrink_k_chunk(int K);   // K elements per chunk (multiple of 256)
+cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, cudaStream_t s);
+
+}  // namespace mlora

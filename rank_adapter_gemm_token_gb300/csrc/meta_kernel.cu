@@ -1,0 +1,176 @@
+// Per-step slot metadata: a stable counting sort of the step's (token, slot) pairs by slot.
+//
+// "Multi-LoRA Serving Explained" (sevydevy.com), batched-serving section: the segmented
+// method orders tokens with a stable argsort of their slot ids and runs one small product
+// per group, so each adapter is read once per group; the same page reports that the vLLM
+// kernel path sorts the batch by slot before shrink and expand, and skips the LoRA kernels
+// when no token uses an adapter. "[RFC] Per-request activation of multiple LoRA adapters"
+// (vLLM issue 51940), Proposed Change item 2: k slots per token, unused ones the sentinel.
+//
+// One CTA of 1024 threads does the whole sort: a shared-memory histogram over the S + 1
+// bins (bin 0 = sentinel), one block-wide exclusive scan (bin starts, segment numbers and
+// pair-block numbers at once), then a scatter in chunks of 1024 pairs in which each pair's
+// rank inside its bin is (pairs of the same bin in earlier chunks) + (in earlier warps of
+// this chunk) + (in earlier lanes of its warp, from __match_any_sync). The result is
+// exactly the stable order; it does not depend on thread timing.
+#include <climits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mlora {
+namespace {
+
+__device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& pa, int& pb, int& pc,
+                                                      int* warp_sums /* [3][32] */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int sa = a, sb = b, sc = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int ta = __shfl_up_sync(0xffffffffu, sa, d), tb = __shfl_up_sync(0xffffffffu, sb, d),
+        tc = __shfl_up_sync(0xffffffffu, sc, d);
+    if (lane >= d) { sa += ta; sb += tb; sc += tc; }
+  }
+  if (lane == 31) { warp_sums[warp] = sa; warp_sums[32 + warp] = sb; warp_sums[64 + warp] = sc; }
+  __syncthreads();
+  if (warp == 0) {
+    int wa = warp_sums[lane], wb = warp_sums[32 + lane], wc = warp_sums[64 + lane];
+    int xa = wa, xb = wb, xc = wc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int ta = __shfl_up_sync(0xffffffffu, xa, d), tb = __shfl_up_sync(0xffffffffu, xb, d),
+          tc = __shfl_up_sync(0xffffffffu, xc, d);
+      if (lane >= d) { xa += ta; xb += tb; xc += tc; }
+    }
+    warp_sums[lane] = xa - wa; warp_sums[32 + lane] = xb - wb; warp_sums[64 + lane] = xc - wc;
+  }
+  __syncthreads();
+  pa = warp_sums[warp] + sa - a;
+  pb = warp_sums[32 + warp] + sb - b;
+  pc = warp_sums[64 + warp] + sc - c;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kMetaThreads, 1)
+build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, int S,
+                  const int32_t* __restrict__ slot_rank, MetaView m) {
+  extern __shared__ int smem[];
+  const int nb = S + 1;
+  int* hist = smem;                          // [nb] pairs per bin
+  int* cursor = hist + nb;                   // [nb] next free position of each bin
+  int* chunk_tot = cursor + nb;              // [nb] pairs per bin in the current chunk
+  uint16_t* wcnt = reinterpret_cast<uint16_t*>(chunk_tot + nb);   // [32][nb]
+  __shared__ int warp_sums[96];
+  __shared__ int first_bad;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int b = tid; b < nb; b += kMetaThreads) hist[b] = 0;
+  if (tid == 0) first_bad = INT_MAX;
+  __syncthreads();
+
+  // 1. validate, histogram, per-pair slot and scale
+  for (int p = tid; p < n; p += kMetaThreads) {
+    int s = token_slots[p];
+    const bool ok = (s == -1) || (s >= 0 && s < S && slot_rank[s] > 0);
+    if (!ok) {
+      atomicMin(&first_bad, p);
+      s = -1;
+    }
+    m.pair_slot[p] = s;
+    m.pair_scale[p] = (s < 0) ? 0.0f : (scales ? scales[p] : 1.0f);
+    atomicAdd(&hist[s + 1], 1);
+  }
+  __syncthreads();
+
+  // 2. one scan for bin starts, segment numbers and pair-block numbers
+  const int per = (nb + kMetaThreads - 1) / kMetaThreads;
+  const int b0 = min(tid * per, nb), b1 = min(b0 + per, nb);
+  int h = 0, f = 0, k = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int c = hist[b];
+    h += c;
+    f += c > 0;
+    if (b > 0) k += (c + kPairBlock - 1) / kPairBlock;
+  }
+  int ph, pf, pk;
+  block_exclusive_scan3(h, f, k, ph, pf, pk, warp_sums);
+  for (int b = b0; b < b1; ++b) {
+    const int c = hist[b];
+    cursor[b] = ph;
+    if (c > 0) {
+      m.seg_slot[pf] = b - 1;
+      m.seg_off[pf] = ph;
+      ++pf;
+      if (b > 0) {
+        for (int i = 0; i * kPairBlock < c; ++i, ++pk) {
+          m.blk_slot[pk] = b - 1;
+          m.blk_start[pk] = ph + i * kPairBlock;
+          m.blk_count[pk] = min(kPairBlock, c - i * kPairBlock);
+        }
+      }
+    }
+    ph += c;
+  }
+  if (b1 == nb && b0 < b1) {                 // the thread owning the last bin holds the totals
+    m.seg_off[pf] = n;
+    m.counts[0] = pf;
+    m.counts[1] = n - hist[0];
+    m.counts[2] = pk;
+  }
+  __syncthreads();
+
+  // 3. stable scatter, 1024 pairs per chunk
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < n; base += kMetaThreads) {
+    for (int i = tid; i < 32 * nb; i += kMetaThreads) wcnt[i] = 0;
+    __syncthreads();
+    const int p = base + tid;
+    const bool valid = p < n;
+    const int bin = valid ? m.pair_slot[p] + 1 : nb;      // nb = "no pair" (never stored)
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    const int rank_in_warp = __popc(peers & lt_mask);
+    if (valid && lane == __ffs(peers) - 1) wcnt[warp * nb + bin] = static_cast<uint16_t>(__popc(peers));
+    __syncthreads();
+    for (int b = tid; b < nb; b += kMetaThreads) {
+      int run = 0;
+      for (int w = 0; w < 32; ++w) {
+        const int c = wcnt[w * nb + b];
+        wcnt[w * nb + b] = static_cast<uint16_t>(run);
+        run += c;
+      }
+      chunk_tot[b] = run;
+    }
+    __syncthreads();
+    if (valid) m.order[cursor[bin] + wcnt[warp * nb + bin] + rank_in_warp] = p;
+    __syncthreads();
+    for (int b = tid; b < nb; b += kMetaThreads) cursor[b] += chunk_tot[b];
+    __syncthreads();
+  }
+
+  if (tid == 0) {
+    m.counts[3] = first_bad;
+    if (first_bad != INT_MAX) atomicOr(m.err, ptx::kErrBadSlot);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
+                              const int32_t* slot_rank, const MetaView& m, cudaStream_t s) {
+  const int nb = S + 1;
+  const size_t smem = static_cast<size_t>(nb) * (3 * sizeof(int) + 32 * sizeof(uint16_t));
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kMaxSlots + 1) * (3 * sizeof(int) + 32 * sizeof(uint16_t))));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  note_launch_begin(kKindMeta, s);
+  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, T * J, S, slot_rank, m);
+  cudaError_t e = cudaGetLastError();
+  note_launch_end(kKindMeta, s);
+  return e;
+}
+
+}  // namespace mlora

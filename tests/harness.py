@@ -1,0 +1,102 @@
+"""Glue for GPU tests and the benchmark: puts a synthetic workload on the device through the
+library's API, and compares device outputs with the fp64 oracle."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle
+import synth
+
+# Tolerances for bf16 inputs with fp32 accumulation (per linear output tensor).
+REL_FROB_TOL = 5e-3
+MAX_ABS_TOL = 3e-2
+
+
+def errors(y_dev: np.ndarray, y_ref: np.ndarray) -> tuple:
+    diff = y_dev.astype(np.float64) - y_ref
+    den = np.linalg.norm(y_ref)
+    rel = float(np.linalg.norm(diff) / den) if den > 0 else float(np.linalg.norm(diff))
+    return rel, float(np.max(np.abs(diff))) if diff.size else 0.0
+
+
+def assert_close(y_dev, y_ref, what: str, rel_tol: float = REL_FROB_TOL, abs_tol: float = MAX_ABS_TOL):
+    rel, mx = errors(np.asarray(y_dev), np.asarray(y_ref))
+    assert rel <= rel_tol and mx <= abs_tol, f"{what}: rel Frobenius {rel:.3e} (tol {rel_tol}), max abs {mx:.3e} (tol {abs_tol})"
+    return rel, mx
+
+
+@dataclass
+class DeviceLinear:
+    lin: synth.Linear
+    pool: object
+    W: object
+    y: object
+
+
+class DeviceWorkload:
+    """A synth.Workload resident on the GPU: one pool per linear, W, x, token slots, scales."""
+
+    def __init__(self, wl: synth.Workload, device="cuda:0", linears=None):
+        import torch
+        from rank_adapter_gemm_token_gb300 import layer
+
+        self.torch = torch
+        self.layer = layer
+        self.wl = wl
+        self.device = torch.device(device)
+        self.meta = layer.StepMeta(max(wl.T, 1), wl.J, wl.r_max)
+        self.token_slots = torch.from_numpy(np.ascontiguousarray(wl.token_slots.astype(np.int32))).to(self.device)
+        self.scales = None if wl.scales is None else torch.from_numpy(
+            np.ascontiguousarray(wl.scales.astype(np.float32))).to(self.device)
+        self.x = {k: layer.bf16_from_bits(v, self.device) for k, v in wl.xs.items()}
+        self.linears = []
+        for lin in (wl.linears if linears is None else linears):
+            pool = layer.AdapterPool(wl.n_slots, wl.r_max, lin.K, lin.D)
+            for s, ad in lin.adapters.items():
+                pool.load(s, ad.A, ad.B, ad.rank, ad.alpha, ad.rslora)
+            W = layer.bf16_from_bits(lin.W, self.device)
+            y = torch.empty((wl.T, lin.D), dtype=torch.float32, device=self.device)
+            self.linears.append(DeviceLinear(lin, pool, W, y))
+        for dl in self.linears:
+            dl.pool.sync()
+
+    def build_meta(self, stream=None):
+        self.meta.build(self.token_slots, self.scales, self.linears[0].pool, stream)
+
+    def run(self, stream=None):
+        """One step: build the metadata once, then every linear of the workload."""
+        self.build_meta(stream)
+        for dl in self.linears:
+            self.layer.linear(dl.pool, self.meta, self.x[dl.lin.x_id], dl.W, dl.y, stream)
+
+    def close(self):
+        for dl in self.linears:
+            dl.pool.close()
+        self.meta.close()
+
+
+def oracle_rows(wl: synth.Workload, lin: synth.Linear, rows=None, cols=None, threads=None) -> np.ndarray:
+    return oracle.linear(wl.xs[lin.x_id], lin.W, wl.token_slots, lin.adapters, wl.n_slots, scales=wl.scales,
+                         rows=rows, cols=cols, threads=threads)
+
+
+def sample_rows(wl: synth.Workload, n: int, seed: int = 0) -> np.ndarray:
+    """n token rows covering sentinel rows, both ends and a spread of slots (sorted)."""
+    T = wl.T
+    rng = np.random.default_rng(seed)
+    picks = {0, T - 1}
+    flat = wl.token_slots
+    sent = np.where(np.all(flat < 0, axis=1))[0]
+    if len(sent):
+        picks.add(int(sent[0]))
+    seen = set()
+    for t in range(T):                       # first token of each distinct first slot
+        s = int(flat[t, 0])
+        if s not in seen and len(picks) < n // 2:
+            seen.add(s)
+            picks.add(t)
+    while len(picks) < min(n, T):
+        picks.add(int(rng.integers(0, T)))
+    return np.array(sorted(picks), dtype=np.int64)

@@ -1,0 +1,209 @@
+"""The full layer on the GPU against the fp64 oracle, through the C ABI.
+
+Tolerances: relative Frobenius error <= 5e-3 and max-abs error <= 3e-2 per linear output,
+also applied to the LoRA delta alone (y - base) for the relative error. Rows whose slots
+are all -1 must equal the base product bit for bit."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.conftest import read_golden
+from tests.harness import DeviceWorkload, assert_close, errors, oracle_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_linear(wl, dw, dl, rows=None, check_delta=True):
+    from rank_adapter_gemm_token_gb300 import layer
+    y = dl.y.cpu().numpy()
+    ref = oracle_rows(wl, dl.lin, rows=rows)
+    ysel = y if rows is None else y[rows]
+    assert_close(ysel, ref, f"{wl.name}/{dl.lin.name}")
+    base_dev = layer.base_gemm(dw.x[dl.lin.x_id], dl.W).cpu().numpy()
+    bsel = base_dev if rows is None else base_dev[rows]
+    # rows with no active slot equal the base product exactly
+    slots = wl.token_slots if rows is None else wl.token_slots[rows]
+    idle = np.all(slots < 0, axis=1)
+    assert np.array_equal(ysel[idle], bsel[idle]), "sentinel rows differ from the base product"
+    if check_delta and (~idle).any():
+        base_ref = oracle.linear(wl.xs[dl.lin.x_id], dl.lin.W, np.full((wl.T, 1), -1), {}, wl.n_slots, rows=rows)
+        rel, _ = errors(ysel[~idle] - bsel[~idle], ref[~idle] - base_ref[~idle])
+        assert rel <= 5e-3, f"LoRA delta alone: rel Frobenius {rel:.3e}"
+
+
+def test_hand_example_is_bit_exact(cuda_device):
+    """The hand-worked two-slot example, zero-padded to K = D = 8: every value is exact in fp32,
+    so the GPU must reproduce the hand-computed outputs exactly."""
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer
+    g = {k: v for k, v in read_golden("hand_two_slot_rslora.txt") if k != "slot"}
+    slot_lines = [v for k, v in read_golden("hand_two_slot_rslora.txt") if k == "slot"]
+    T, K0, D0, J = (int(g[k][0]) for k in ("T", "K", "D", "J"))
+    K = D = 8
+    f = lambda k: np.array([float(v) for v in g[k]], dtype=np.float32)  # noqa: E731
+    bits = lambda a: (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)  # noqa: E731
+    x = np.zeros((T, K), np.float32); x[:, :K0] = f("x").reshape(T, K0)
+    W = np.zeros((D, K), np.float32); W[:D0, :K0] = f("W").reshape(D0, K0)
+    pool = layer.AdapterPool(int(g["n_slots"][0]), 4, K, D)
+    for sl in slot_lines:
+        s = int(sl[0]); kv = dict(zip(sl[1::2], sl[2::2])); r = int(kv["rank"])
+        A = np.zeros((r, K), np.float32); A[:, :K0] = f(f"A{s}").reshape(r, K0)
+        B = np.zeros((D, r), np.float32); B[:D0] = f(f"B{s}").reshape(D0, r)
+        pool.load(s, bits(A), bits(B), r, float(kv["alpha"]), bool(int(kv["rslora"])))
+    pool.sync()
+    meta = layer.StepMeta(T, J, 4)
+    ts = torch.tensor(np.array([int(v) for v in g["token_slots"]], np.int32).reshape(T, J), device="cuda")
+    sc = torch.tensor(f("scales").reshape(T, J), device="cuda")
+    meta.build(ts, sc, pool)
+    y = layer.linear(pool, meta, layer.bf16_from_bits(bits(x), "cuda"), layer.bf16_from_bits(bits(W), "cuda"))
+    meta.status()
+    expect = np.zeros((T, D)); expect[:, :D0] = f("y").reshape(T, D0)
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), expect)
+
+
+def test_tiny_config(cuda_device):
+    wl = synth.tiny()
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
+    dw.close()
+
+
+@pytest.mark.parametrize("T,K,D,S,R,J,seed", [(300, 200, 520, 7, 16, 2, 0), (129, 264, 136, 3, 64, 1, 1),
+                                              (77, 64, 8, 12, 8, 3, 2), (513, 1024, 384, 40, 24, 2, 3)])
+def test_ragged_multi_slot_cases(cuda_device, T, K, D, S, R, J, seed):
+    """Several tiles with ragged tails, mixed ranks below r_max, rsLoRA, J slots with sentinels."""
+    rng = np.random.default_rng(seed)
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = int(rng.integers(1, R + 1))
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(seed, 300 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(rng.integers(1, 3 * r)), rslora=bool(s % 3 == 0))
+    slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    slots[::5, :] = -1
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("ragged", seed, T, J, S, R, slots, scales, {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
+    dw.close()
+
+
+def test_decode_config_full_size(cuda_device):
+    wl = synth.decode()
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    rows = sample_rows(wl, 24)
+    for dl in dw.linears:
+        _check_linear(wl, dw, dl, rows=rows)
+    dw.close()
+
+
+def test_compose_config_full_size(cuda_device):
+    wl = synth.compose()
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    rows = sample_rows(wl, 32)
+    _check_linear(wl, dw, dw.linears[0], rows=rows)
+    # RFC 51940, Testing: the fused k-slot pass equals running one slot at a time and accumulating.
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer
+    dl = dw.linears[0]
+    fused = dl.y.clone()
+    acc = layer.base_gemm(dw.x[0], dl.W)
+    meta1 = layer.StepMeta(wl.T, 1, wl.r_max)
+    for j in range(wl.J):
+        meta1.build(dw.token_slots[:, j].contiguous().view(wl.T, 1), dw.scales[:, j].contiguous(), dl.pool)
+        layer.linear(dl.pool, meta1, dw.x[0], dl.W, dl.y)
+        acc += dl.y - layer.base_gemm(dw.x[0], dl.W)
+    rel, mx = errors(fused.cpu().numpy(), acc.cpu().numpy().astype(np.float64))
+    assert rel < 1e-5 and mx < 1e-4, (rel, mx)
+    dw.close()
+
+
+def test_prefill_config_full_size(cuda_device):
+    wl = synth.prefill()
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    rows = sample_rows(wl, 16)
+    for dl in dw.linears:
+        _check_linear(wl, dw, dl, rows=rows)
+    dw.close()
+
+
+def test_zero_scale_and_linearity_on_gpu(cuda_device):
+    import torch
+    wl = synth.compose(T=64)
+    dw = DeviceWorkload(wl)
+    outs = {}
+    for s in (0.0, 1.0, 0.5):
+        dw.scales = torch.full((wl.T, wl.J), s, dtype=torch.float32, device="cuda")
+        dw.run()
+        outs[s] = dw.linears[0].y.cpu().numpy().astype(np.float64)
+    from rank_adapter_gemm_token_gb300 import layer
+    base = layer.base_gemm(dw.x[0], dw.linears[0].W).cpu().numpy()
+    assert np.array_equal(outs[0.0], base)                  # zero scale adds exact zeros
+    rel, _ = errors(outs[0.5] - base, 0.5 * (outs[1.0] - base))
+    assert rel < 1e-6
+    dw.close()
+
+
+def test_reload_slot_after_use(cuda_device):
+    """Write-after-read: reloading a slot that a queued linear still reads must not change that
+    linear's result, and the next linear sees the new adapter."""
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer
+    wl = synth.tiny(T=64)
+    dw = DeviceWorkload(wl)
+    dl = dw.linears[0]
+    y_first = torch.empty_like(dl.y)
+    dw.build_meta()
+    layer.linear(dl.pool, dw.meta, dw.x[0], dl.W, y_first)
+    new = synth.Adapter(A=synth.normal_bf16(99, 1, (8, wl.linears[0].K), 0.02),
+                        B=synth.normal_bf16(99, 2, (wl.linears[0].D, 8), 0.02), rank=8, alpha=8.0)
+    dl.pool.load(1, new.A, new.B, new.rank, new.alpha, new.rslora)
+    layer.linear(dl.pool, dw.meta, dw.x[0], dl.W, dl.y)
+    torch.cuda.synchronize()
+    rows = np.arange(wl.T)
+    assert_close(y_first.cpu().numpy(), oracle_rows(wl, wl.linears[0], rows=rows), "before reload")
+    wl.linears[0].adapters[1] = new
+    assert_close(dl.y.cpu().numpy(), oracle_rows(wl, wl.linears[0], rows=rows), "after reload")
+    dw.close()
+
+
+def test_load_errors(cuda_device):
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    pool = layer.AdapterPool(4, 16, 64, 64)
+    A = np.zeros((32, 64), np.uint16)
+    B = np.zeros((64, 32), np.uint16)
+    with pytest.raises(mlora.MloraError) as e:
+        pool.load(0, A, B, 32, 64.0)
+    assert e.value.status == mlora.MLORA_ERR_RANK_TOO_LARGE and "32" in str(e.value) and "16" in str(e.value)
+    with pytest.raises(mlora.MloraError) as e:
+        pool.load(4, A[:8], B[:, :8], 8, 16.0)
+    assert e.value.status == mlora.MLORA_ERR_SLOT_RANGE
+    with pytest.raises(mlora.MloraError) as e:
+        mlora.mlora_load_adapter(pool.handle, 0, A[:8], np.ascontiguousarray(B[:, :8]), 8, float("nan"), 0)
+    assert e.value.status == mlora.MLORA_ERR_RANK_INVALID
+    pool.close()
+
+
+def test_clear_slot_makes_it_empty(cuda_device):
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    wl = synth.tiny()
+    dw = DeviceWorkload(wl)
+    dw.linears[0].pool.clear(2)
+    dw.run()
+    if (wl.token_slots == 2).any():
+        with pytest.raises(mlora.MloraError) as e:
+            dw.meta.status()
+        assert e.value.status == mlora.MLORA_ERR_BAD_TOKEN_SLOT
+    dw.close()
