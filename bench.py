@@ -101,52 +101,70 @@ def algorithmic_bytes(wl) -> dict:
 
 # ------------------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock, its maximum and the clock-event (throttle) reasons through NVML
+    (ctypes, read-only queries) from a thread every ~0.5 ms while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
-        self.gpu = gpu_index
+    def __init__(self, cuda_index: int):
+        import threading
+        self.samples, self.error, self.h = [], None, None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import ctypes
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+                u = getattr(torch.cuda.get_device_properties(cuda_index), "uuid", None)
+                if u is not None:
+                    uuid = "GPU-" + str(u)
+            except Exception:
+                pass
+            ok = uuid is not None and self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            if not ok and self.nvml.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.h = h
+        except OSError as e:
+            self.error = str(e)
+
+    def _run(self):
+        import ctypes
+        mhz, mx, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if (self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0 and
+                    self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 and
+                    get_reasons(self.h, ctypes.byref(mask)) == 0):
+                self.samples.append((mhz.value, mx.value, mask.value))
+            time.sleep(0.0005)
 
     def start(self):
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        import threading
+        if self.h is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if self._thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"NVML unavailable: {self.error}"]}
+        self._stop.set()
+        self._thread.join()
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = set()
+        for _, _, m in self.samples:
+            for bit, name in self.REASONS.items():
+                if m & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([s[0] for s in self.samples])),
+                "sm_max_mhz": float(max(s[1] for s in self.samples)), "samples": len(self.samples),
+                "reasons": sorted(reasons), "source": "NVML, sampled during the timed steps"}
 
 
 # ------------------------------------------------------------------------------ oracle timing
@@ -289,8 +307,9 @@ def run_ours(args):
     value = ws * wl.T / (ms / 1000.0)
 
     # ---- per-kernel durations: the same K steps again with the library's event trace
-    mlora.mlora_trace_enable(64 * args.steps + 64)
-    for i in range(args.steps):
+    trace_steps = min(args.steps, 100)
+    mlora.mlora_trace_enable(64 * trace_steps + 64)
+    for i in range(trace_steps):
         flush.zero_()
         dw.run(stream)
     barrier()
@@ -337,7 +356,7 @@ def run_ours(args):
     dom = max(kinds, key=lambda k: kinds[k][1])
     n_launch, tot_ms = kinds[dom]
     avg_s = tot_ms / n_launch / 1000.0
-    launches_per_step = n_launch / args.steps
+    launches_per_step = n_launch / trace_steps
     if dom == "base_gemm":
         flops = algo["base_flops"] / launches_per_step
         byts = algo["base_gemm"] / launches_per_step
@@ -357,7 +376,7 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": byts, "avg_launch_us": avg_s * 1e6}
     per_kernel = {}
     for k, (n, t) in kinds.items():
-        per = n / args.steps
+        per = n / trace_steps
         entry = {"launches_per_step": per, "avg_us": 1000.0 * t / n, "share": t / sum(v[1] for v in kinds.values())}
         if k in algo and algo[k] > 0:
             entry["achieved_GBps"] = algo[k] / per / (t / n / 1000.0) / 1e9
@@ -385,7 +404,7 @@ def run_ours(args):
         "clocks": clock_info,
         "kernels": per_kernel,
         "wall_s_timed_region": wall,
-        "kernel_timing": "second pass of the same K steps with per-kernel CUDA events on the launch stream",
+        "kernel_timing": f"second pass of {trace_steps} steps with per-kernel CUDA events on the launch stream",
     }
     print(json.dumps(line), flush=True)
     dw.close()
@@ -398,7 +417,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "compose", "tiny"])

@@ -16,6 +16,7 @@
 // Tiles are visited M-fastest so that the CTAs working on one W column block run together
 // and W is read from HBM once. Every wait is bounded (2 s): on a timeout the kernel sets
 // an error bit and leaves instead of hanging.
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <cstdio>
@@ -183,6 +184,150 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Skinny variant for small batches (T <= 256, the decode case): the roles swap so that W is the
+// A operand (128 output features per CTA, M = 128) and all tokens form N (NT = T rounded up to
+// 16), which reads every W element exactly once. K is split across the CTAs of a thread-block
+// cluster (cluster rank = K split); each CTA stages its fp32 partial tile P[t][o] in its own
+// shared memory, and after a cluster barrier CTA r sums the partials of all CTAs for its share
+// of the tokens through distributed shared memory, always in rank order 0, 1, ... (so the
+// result is deterministic), and writes y with coalesced 16-byte stores.
+constexpr int kSkinnyStages = 4;
+constexpr int kSkinnyABytes = BM * BK * 2;
+
+__host__ __device__ constexpr int skinny_stage_bytes(int NT) { return kSkinnyABytes + NT * BK * 2; }
+__host__ __device__ constexpr int skinny_smem_bytes(int NT) {
+  return kSkinnyStages * skinny_stage_bytes(NT) + 256 + 1024;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                        float* __restrict__ y, int T, int D, int K, int NT, int splitk, uint32_t tmem_cols,
+                        uint32_t* __restrict__ err) {
+  namespace cg = cooperative_groups;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_bytes = skinny_stage_bytes(NT);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkinnyStages * stage_bytes);
+  uint64_t* empty = full + kSkinnyStages;
+  uint64_t* acc_full = empty + kSkinnyStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  float* part = reinterpret_cast<float*>(smem);          // [NT][128] after the main loop
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int oblk = blockIdx.x / splitk;
+  const int ks = static_cast<int>(cluster.block_rank());
+  const int o0 = oblk * BM;
+  const int num_kb = (K + BK - 1) / BK;
+  const int kb0 = ks * num_kb / splitk, kb1 = (ks + 1) * num_kb / splitk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSkinnyStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+    ptx::tma_prefetch_desc(&tmap_w);
+    ptx::tma_prefetch_desc(&tmap_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) break;
+        uint8_t* sa = smem + stage * stage_bytes;
+        ptx::mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
+        ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
+        ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
+        if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, NT);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool mma_ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!ptx::mbar_wait(&full[stage], phase, err)) { mma_ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t a_addr = ptx::smem_u32(smem + stage * stage_bytes);
+        const uint64_t a_desc = ptx::sw128_kmajor_desc(a_addr);
+        const uint64_t b_desc = ptx::sw128_kmajor_desc(a_addr + kSkinnyABytes);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          ptx::umma_bf16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        ptx::umma_commit(&empty[stage]);
+        if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
+      }
+      if (mma_ok) ptx::umma_commit(acc_full);
+    }
+  } else {
+    // TMEM lane = output feature o (warp w reads lanes 32*(w%4)..), columns = tokens
+    const int quarter = warp & 3;
+    const int o = quarter * 32 + lane;
+    if (ptx::mbar_wait(acc_full, 0, err)) {
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c), r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part[(c + i) * BM + o] = __uint_as_float(r[i]);
+      }
+    } else {
+      ok = false;
+    }
+  }
+  ptx::tc_fence_before();
+  cluster.sync();                                     // every partial tile is in shared memory
+
+  // Reduction: CTA ks owns tokens [t0, t1); float4 over o, partials summed in rank order.
+  const int per = (T + splitk - 1) / splitk;
+  const int t0 = ks * per, t1 = min(T, t0 + per);
+  for (int i = threadIdx.x; i < (t1 - t0) * (BM / 4); i += kGemmThreads) {
+    const int t = t0 + i / (BM / 4);
+    const int o4 = (i % (BM / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < splitk; ++r) {
+      const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int o = o0 + o4;
+    float* dst = y + static_cast<size_t>(t) * D + o;
+    if (o + 4 <= D && (D & 3) == 0) {
+      *reinterpret_cast<float4*>(dst) = acc;
+    } else {
+      if (o < D) dst[0] = acc.x;
+      if (o + 1 < D) dst[1] = acc.y;
+      if (o + 2 < D) dst[2] = acc.z;
+      if (o + 3 < D) dst[3] = acc.w;
+    }
+  }
+  (void)ok;
+  cluster.sync();                                     // no CTA leaves while others read its tile
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -240,11 +385,53 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
   return e;
 }
 
+cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                          int num_sms, cudaStream_t s) {
+  const int NT = (T + 15) / 16 * 16;
+  const int n_oblk = (D + BM - 1) / BM;
+  const int num_kb = (K + BK - 1) / BK;
+  int splitk = num_sms / n_oblk;
+  if (splitk > 8) splitk = 8;
+  if (splitk > num_kb) splitk = num_kb;
+  if (splitk < 1) splitk = 1;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(NT)) tmem_cols <<= 1;
+  const int smem = skinny_smem_bytes(NT);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         skinny_smem_bytes(256));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  CUtensorMap mw, mx;
+  if (!make_tmap_bf16(&mw, W, D, K, BM, BK) || !make_tmap_bf16(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_oblk * splitk, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = splitk;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launch_begin(kKindGemm, s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, y, T, D, K, NT, splitk, tmem_cols, err);
+  note_launch_end(kKindGemm, s);
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                              uint32_t* err, int num_sms, cudaStream_t s) {
   if (T == 0 || D == 0) return cudaSuccess;
+  if (T <= 256) return launch_skinny(x, W, y, T, K, D, err, num_sms, s);
   // Largest N tile that still gives every SM a tile; small problems take N = 64.
   const int m_tiles = (T + BM - 1) / BM;
   if (m_tiles * ((D + 255) / 256) >= num_sms) return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, s);

@@ -11,7 +11,6 @@ constexpr int kMaxSlots = 2048;     // pool slots (GPU-resident adapters)
 constexpr int kMaxRank = 256;       // r_max
 constexpr int kMaxJ = 8;            // adapter slots per token
 constexpr int kPairBlock = 16;      // pairs of one slot handled together by the shrink
-constexpr int kShrinkSplits = 8;    // K is cut into at most this many chunks by the shrink
 constexpr int kMetaThreads = 1024;
 
 // Device arrays of one adapter pool (one adapted linear).
@@ -35,7 +34,7 @@ struct MetaView {
   int32_t* blk_count;   // [n]   pairs in the block
   int32_t* counts;      // [4] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none)
   uint32_t* err;        // device error word (ptx::kErr* bits)
-  float* vpart;         // shrink output: [n_kchunks][n][R] fp32 partial sums over K chunks
+  float* vpart;         // shrink output v: [n][R] fp32 (unscaled A x per pair)
   int n;                // pairs of the current step (T * J)
   int T, J;
 };
@@ -55,9 +54,8 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                              uint32_t* err, int num_sms, cudaStream_t s);
 
-int shrink_k_chunk(int K);   // K elements per chunk (multiple of 256)
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
                                cudaStream_t s);
-cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, cudaStream_t s);
+cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s);
 
 }  // namespace mlora

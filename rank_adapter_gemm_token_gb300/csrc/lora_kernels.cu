@@ -8,23 +8,24 @@
 // -1 skipped, each weighted by its own scale, iterated inside one fused pass. "[vLLM] LoRA"
 // (secrett2633 blog), PEFTHelper: the slot factor is alpha/r, alpha/sqrt(r) under rsLoRA.
 //
-// Shrink works per pair-block (at most 16 pairs of one slot, from the sorted metadata) and
-// per K chunk: a warp owns one adapter row q, streams A[slot][q][chunk] once with 16-byte
-// loads and reuses it for every pair of the block, writing fp32 partial sums
-// vpart[chunk][p][q] (unscaled). Expand works per token and D range: it sums the chunk
-// partials in a fixed order, multiplies by pair scale * slot factor, and adds the slot's
-// B rows (16-byte loads, zero padding beyond the true rank skipped) into y in slot order
-// j = 0..J-1, so every output is deterministic. Tokens whose slots are all -1 are never
-// touched, and when the step has no active pair no block does any work.
+// Shrink works per pair-block (at most 16 pairs of one slot, from the sorted metadata): each
+// warp streams one row of A[slot] over the whole K range once with 16-byte loads, reusing each
+// vector for the pairs of the block, and writes the unscaled fp32 v[p][q]. Expand multiplies
+// v by the pair's scale times the slot factor. With one slot per token it works per pair-block and
+// 512-column range: B[slot] rows are read once per block (thread = output column, so both
+// the B rows and y are accessed coalesced) and each y element receives exactly one update.
+// With several slots per token it works per token, adding the slots in order j = 0..J-1.
+// Either way every output is a fixed sequence of fp32 operations (deterministic), tokens
+// whose slots are all -1 are never touched, and with no active pair no block does any work.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace mlora {
 namespace {
 
-constexpr int kShrinkThreads = 256;
-constexpr int kExpandThreads = 256;
-constexpr int kExpandCols = 8;            // outputs per thread
+constexpr int kShrinkThreads = 512;      // 16 warps; a warp owns one adapter row at a time
+constexpr int kExpandThreads = 256;      // one output column per thread, coalesced B rows and y
+constexpr int kExpandColsPerItem = 512;  // two columns per thread per item
 
 __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
   float s = ptx::bf16_lo(a.x) * ptx::bf16_lo(b.x);
@@ -38,151 +39,201 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
   return s;
 }
 
-__global__ void __launch_bounds__(kShrinkThreads)
-lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, int kc_len, int n_kc) {
+__device__ __forceinline__ float dot8_bf16_f32(const uint4& b, const float* v) {
+  float a = ptx::bf16_lo(b.x) * v[0];
+  a = fmaf(ptx::bf16_hi(b.x), v[1], a);
+  a = fmaf(ptx::bf16_lo(b.y), v[2], a);
+  a = fmaf(ptx::bf16_hi(b.y), v[3], a);
+  a = fmaf(ptx::bf16_lo(b.z), v[4], a);
+  a = fmaf(ptx::bf16_hi(b.z), v[5], a);
+  a = fmaf(ptx::bf16_lo(b.w), v[6], a);
+  a = fmaf(ptx::bf16_hi(b.w), v[7], a);
+  return a;
+}
+
+// Item = one pair-block (at most 16 pairs of one slot). Warp w owns adapter rows w, w + 16, ...
+// and covers the whole K range: lane l reads 8-element vectors l, l + 32, ... of the row with
+// 16-byte loads (eight in flight per lane), reusing each vector for a group of 4 pairs from
+// registers; a warp shuffle then gives the final dot products, so v needs no cross-CTA sum.
+__global__ void __launch_bounds__(kShrinkThreads, 1)
+lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m) {
+  constexpr int G = 4;                                        // pairs per register group
+  constexpr int U = 8;                                        // vector steps in flight per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_blocks = m.counts[2];
-  const int items = n_blocks * n_kc;
   const int K = pool.K, R = pool.R;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int b = item / n_kc, kc = item - b * n_kc;
+  const int nvec = K / 8;
+  for (int b = blockIdx.x; b < n_blocks; b += gridDim.x) {
     const int slot = m.blk_slot[b];
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
-    const int k0 = kc * kc_len;
-    const int k1 = min(K, k0 + kc_len);
-    int tok[kPairBlock];
-    int pr[kPairBlock];
-#pragma unroll
-    for (int i = 0; i < kPairBlock; ++i) {
-      pr[i] = i < cnt ? m.order[start + i] : 0;
-      tok[i] = pr[i] / m.J;
-    }
     for (int q = warp; q < rank; q += kShrinkThreads / 32) {
-      const uint16_t* arow = pool.A + (static_cast<size_t>(slot) * R + q) * K;
-      float acc[kPairBlock];
+      const uint4* arow = reinterpret_cast<const uint4*>(pool.A + (static_cast<size_t>(slot) * R + q) * K);
+      for (int g0 = 0; g0 < cnt; g0 += G) {
+        const int gc = min(G, cnt - g0);
+        int pr[G];
+        const uint4* xv[G];
 #pragma unroll
-      for (int i = 0; i < kPairBlock; ++i) acc[i] = 0.f;
-      for (int k = k0 + lane * 8; k < k1; k += 256) {
-        const uint4 av = *reinterpret_cast<const uint4*>(arow + k);
+        for (int i = 0; i < G; ++i) {
+          pr[i] = m.order[start + g0 + (i < gc ? i : 0)];
+          xv[i] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(pr[i] / m.J) * K);
+        }
+        float acc[G];
 #pragma unroll
-        for (int i = 0; i < kPairBlock; ++i) {
-          if (i < cnt) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(tok[i]) * K + k);
-            acc[i] += dot8_bf16(av, xv);
+        for (int i = 0; i < G; ++i) acc[i] = 0.f;
+        int u = lane;
+        for (; u + 32 * (U - 1) < nvec; u += 32 * U) {
+          uint4 a[U];
+#pragma unroll
+          for (int k = 0; k < U; ++k) a[k] = __ldg(arow + u + 32 * k);
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            if (i < gc) {
+              float s = 0.f;
+#pragma unroll
+              for (int k = 0; k < U; ++k) s += dot8_bf16(a[k], __ldg(xv[i] + u + 32 * k));
+              acc[i] += s;
+            }
           }
         }
-      }
+        for (; u < nvec; u += 32) {
+          const uint4 a0 = __ldg(arow + u);
 #pragma unroll
-      for (int i = 0; i < kPairBlock; ++i) {
-        float v = acc[i];
+          for (int i = 0; i < G; ++i)
+            if (i < gc) acc[i] += dot8_bf16(a0, __ldg(xv[i] + u));
+        }
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-        if (lane == 0 && i < cnt) m.vpart[(static_cast<size_t>(kc) * m.n + pr[i]) * R + q] = v;
+        for (int i = 0; i < G; ++i) {
+          float v = acc[i];
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+          if (lane == 0 && i < gc) m.vpart[static_cast<size_t>(pr[i]) * R + q] = v;
+        }
       }
     }
   }
 }
 
+// v of pair p (unscaled shrink output) times coef, zero beyond the rank.
+__device__ __forceinline__ float pair_v(const MetaView& m, int R, int p, int q, int rank, float coef) {
+  return q < rank ? coef * m.vpart[static_cast<size_t>(p) * R + q] : 0.f;
+}
+
+// J == 1: item = (pair-block, 512-column range). The block's scaled v rows sit in shared memory;
+// thread c reads B[slot] row o (consecutive threads -> consecutive rows, coalesced) once and
+// updates y[t][o] for every token of the block (consecutive o, coalesced). Each y element is
+// updated by exactly one pair, so the result is deterministic.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_kc) {
-  __shared__ float vs[kMaxJ][kMaxRank];
+lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+  __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
+  __shared__ int tok[kPairBlock];
+  const int items = m.counts[2] * n_dchunk;
+  const int R = pool.R, D = pool.D;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / n_dchunk, dc = item - b * n_dchunk;
+    const int slot = m.blk_slot[b];
+    const int start = m.blk_start[b];
+    const int cnt = m.blk_count[b];
+    const int rank = pool.slot_rank[slot];
+    const float c = pool.slot_scale[slot];
+    const int rpad = (rank + 7) & ~7;
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
+      const int pi = i / rpad, q = i - pi * rpad;
+      const int p = m.order[start + pi];
+      vs[pi][q] = pair_v(m, R, p, q, rank, c * m.pair_scale[p]);
+      if (q == 0) tok[pi] = p;                      // J == 1: token index == pair index
+    }
+    __syncthreads();
+    for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
+         o += kExpandThreads) {
+      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
+      float d[kPairBlock];
+#pragma unroll
+      for (int i = 0; i < kPairBlock; ++i) d[i] = 0.f;
+      for (int u = 0; u < rpad / 8; ++u) {
+        const uint4 bv = __ldg(brow + u);
+#pragma unroll
+        for (int i = 0; i < kPairBlock; ++i)
+          if (i < cnt) d[i] += dot8_bf16_f32(bv, &vs[i][8 * u]);
+      }
+#pragma unroll
+      for (int i = 0; i < kPairBlock; ++i)
+        if (i < cnt) y[static_cast<size_t>(tok[i]) * D + o] += d[i];
+    }
+  }
+}
+
+// J > 1: item = (token, 512-column range); slots are added in order j = 0..J-1 so every output
+// is a fixed sequence of fp32 additions. Thread c owns column o: B rows and y coalesced.
+__global__ void __launch_bounds__(kExpandThreads)
+lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+  __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
-  const int t = blockIdx.y;
   const int J = m.J, R = pool.R, D = pool.D;
-  bool any = false;
-  for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0;
-  if (!any) return;
-  if (threadIdx.x < J) {
-    const int p = t * J + threadIdx.x;
-    const int s = m.pair_slot[p];
-    ss[threadIdx.x] = s;
-    rs[threadIdx.x] = s >= 0 ? pool.slot_rank[s] : 0;
-    cs[threadIdx.x] = s >= 0 ? m.pair_scale[p] * pool.slot_scale[s] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < J * R; i += kExpandThreads) {
-    const int j = i / R, q = i - j * R;
-    float v = 0.f;
-    if (ss[j] >= 0 && q < rs[j]) {
-      const size_t p = static_cast<size_t>(t) * J + j;
-      for (int kc = 0; kc < n_kc; ++kc) v += m.vpart[(static_cast<size_t>(kc) * m.n + p) * R + q];
+  const int items = m.T * n_dchunk;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int t = item / n_dchunk, dc = item - t * n_dchunk;
+    bool any = false;
+    for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0;
+    if (!any) continue;                                // uniform across the block
+    __syncthreads();
+    if (threadIdx.x < J) {
+      const int p = t * J + threadIdx.x;
+      const int s = m.pair_slot[p];
+      ss[threadIdx.x] = s;
+      rs[threadIdx.x] = s >= 0 ? pool.slot_rank[s] : 0;
+      cs[threadIdx.x] = s >= 0 ? m.pair_scale[p] * pool.slot_scale[s] : 0.f;
     }
-    vs[j][q] = v;
-  }
-  __syncthreads();
-  const int o0 = (blockIdx.x * kExpandThreads + threadIdx.x) * kExpandCols;
-  if (o0 >= D) return;
-  const int ncol = min(kExpandCols, D - o0);
-  float acc[kExpandCols];
-  float* yrow = y + static_cast<size_t>(t) * D + o0;
-#pragma unroll
-  for (int c = 0; c < kExpandCols; ++c) acc[c] = c < ncol ? yrow[c] : 0.f;
-  for (int j = 0; j < J; ++j) {
-    const int s = ss[j];
-    if (s < 0) continue;
-    const int nvec = (rs[j] + 7) / 8;                  // 16-byte vectors covering the true rank
-    float d[kExpandCols];
-#pragma unroll
-    for (int c = 0; c < kExpandCols; ++c) {
-      d[c] = 0.f;
-      if (c < ncol) {
-        const uint16_t* brow = pool.B + (static_cast<size_t>(s) * D + o0 + c) * R;
-        for (int u = 0; u < nvec; ++u) {
-          const uint4 bv = *reinterpret_cast<const uint4*>(brow + 8 * u);
-          const float* v = &vs[j][8 * u];
-          float a = d[c];
-          a = fmaf(ptx::bf16_lo(bv.x), v[0], a);
-          a = fmaf(ptx::bf16_hi(bv.x), v[1], a);
-          a = fmaf(ptx::bf16_lo(bv.y), v[2], a);
-          a = fmaf(ptx::bf16_hi(bv.y), v[3], a);
-          a = fmaf(ptx::bf16_lo(bv.z), v[4], a);
-          a = fmaf(ptx::bf16_hi(bv.z), v[5], a);
-          a = fmaf(ptx::bf16_lo(bv.w), v[6], a);
-          a = fmaf(ptx::bf16_hi(bv.w), v[7], a);
-          d[c] = a;
-        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < J * R; i += kExpandThreads) {
+      const int j = i / R, q = i - j * R;
+      vs[j][q] = ss[j] >= 0 ? pair_v(m, R, t * J + j, q, rs[j], cs[j]) : 0.f;
+    }
+    __syncthreads();
+    for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
+         o += kExpandThreads) {
+      float acc = y[static_cast<size_t>(t) * D + o];
+      for (int j = 0; j < J; ++j) {
+        const int s = ss[j];
+        if (s < 0) continue;
+        const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(s) * D + o) * R);
+        float d = 0.f;
+        for (int u = 0; u < (rs[j] + 7) / 8; ++u) d += dot8_bf16_f32(__ldg(brow + u), &vs[j][8 * u]);
+        acc += d;
       }
+      y[static_cast<size_t>(t) * D + o] = acc;
     }
-#pragma unroll
-    for (int c = 0; c < kExpandCols; ++c) acc[c] = fmaf(cs[j], d[c], acc[c]);
   }
-#pragma unroll
-  for (int c = 0; c < kExpandCols; ++c)
-    if (c < ncol) yrow[c] = acc[c];
 }
 
 }  // namespace
 
-int shrink_k_chunk(int K) {
-  int per = (K + kShrinkSplits - 1) / kShrinkSplits;
-  return ((per + 255) / 256) * 256;
-}
-
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
                                cudaStream_t s) {
   if (m.n == 0) return cudaSuccess;
-  const int kc = shrink_k_chunk(pool.K);
-  const int n_kc = (pool.K + kc - 1) / kc;
-  const int max_items = m.n * n_kc;                     // blocks <= pairs
-  int grid = num_sms * 8;
-  if (grid > max_items) grid = max_items;
+  int grid = num_sms * 2;                                // blocks beyond the pair-block count exit
+  if (grid > m.n) grid = m.n;
   note_launch_begin(kKindShrink, s);
-  lora_shrink_kernel<<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_kc);
+  lora_shrink_kernel<<<grid, kShrinkThreads, 0, s>>>(x, pool, m);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindShrink, s);
   return e;
 }
 
-cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, cudaStream_t s) {
+cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s) {
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
-  const int kc = shrink_k_chunk(pool.K);
-  const int n_kc = (pool.K + kc - 1) / kc;
-  dim3 grid((pool.D + kExpandThreads * kExpandCols - 1) / (kExpandThreads * kExpandCols), m.T);
+  const int n_dchunk = (pool.D + kExpandColsPerItem - 1) / kExpandColsPerItem;
+  const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
+  int grid = num_sms * 8;
+  if (grid > max_items) grid = max_items;
   note_launch_begin(kKindExpand, s);
-  lora_expand_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_kc);
+  if (m.J == 1)
+    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_dchunk);
+  else
+    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_dchunk);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindExpand, s);
   return e;

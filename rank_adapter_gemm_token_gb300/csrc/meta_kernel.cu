@@ -64,14 +64,20 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __shared__ int first_bad;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int b = tid; b < nb; b += kMetaThreads) hist[b] = 0;
+  // 0. which slots hold an adapter (staged once, so pair validation needs no dependent load);
+  //    `cursor` is free until step 2
+  for (int b = tid; b < nb; b += kMetaThreads) {
+    hist[b] = 0;
+    if (b < S) cursor[b] = slot_rank[b] > 0;
+  }
   if (tid == 0) first_bad = INT_MAX;
   __syncthreads();
 
-  // 1. validate, histogram, per-pair slot and scale
+  // 1. validate, histogram, per-pair slot and scale; the first chunk's bins stay in registers
+  int first_bin = nb;
   for (int p = tid; p < n; p += kMetaThreads) {
     int s = token_slots[p];
-    const bool ok = (s == -1) || (s >= 0 && s < S && slot_rank[s] > 0);
+    const bool ok = (s == -1) || (s >= 0 && s < S && cursor[s]);
     if (!ok) {
       atomicMin(&first_bad, p);
       s = -1;
@@ -79,6 +85,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     m.pair_slot[p] = s;
     m.pair_scale[p] = (s < 0) ? 0.0f : (scales ? scales[p] : 1.0f);
     atomicAdd(&hist[s + 1], 1);
+    if (p < kMetaThreads) first_bin = s + 1;
   }
   __syncthreads();
 
@@ -126,7 +133,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     __syncthreads();
     const int p = base + tid;
     const bool valid = p < n;
-    const int bin = valid ? m.pair_slot[p] + 1 : nb;      // nb = "no pair" (never stored)
+    const int bin = !valid ? nb : (base == 0 ? first_bin : m.pair_slot[p] + 1);   // nb = "no pair"
     const unsigned peers = __match_any_sync(0xffffffffu, bin);
     const int rank_in_warp = __popc(peers & lt_mask);
     if (valid && lane == __ffs(peers) - 1) wcnt[warp * nb + bin] = static_cast<uint16_t>(__popc(peers));

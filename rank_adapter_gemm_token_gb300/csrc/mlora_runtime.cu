@@ -18,7 +18,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/mlora.h"
+#include "mlora.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -376,7 +376,7 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->blk_count), n * 4);
   alloc(reinterpret_cast<void**>(&m->counts), 4 * 4);
   alloc(reinterpret_cast<void**>(&m->err), 4);
-  alloc(reinterpret_cast<void**>(&m->vpart), static_cast<size_t>(kShrinkSplits) * n * m->R_max * 4);
+  alloc(reinterpret_cast<void**>(&m->vpart), n * m->R_max * 4);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(m->counts, 0, 16);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->done, cudaEventDisableTiming);
@@ -525,9 +525,11 @@ mlora_status mlora_lora_shrink(mlora_pool_t p, mlora_meta_t m, const mlora_bf16*
 mlora_status mlora_lora_expand(mlora_pool_t p, mlora_meta_t m, float* y, void* stream) {
   if (mlora_status st = check_pair(p, m)) return st;
   if (m->T > 0 && (!y || !aligned16(y))) return fail(MLORA_ERR_INVALID_ARG, "y is NULL or misaligned");
+  DeviceState* ds = nullptr;
+  if (mlora_status st = device_state(&ds)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
-  cudaError_t e = launch_lora_expand(y, p->view(), m->view(), s);
+  cudaError_t e = launch_lora_expand(y, p->view(), m->view(), ds->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "expand launch");
   MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
   MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
@@ -548,7 +550,7 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   const MetaView mv = m->view();
   const PoolView pv = p->view();
   if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "shrink launch");
-  if ((e = launch_lora_expand(y, pv, mv, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
+  if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
   MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
   MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
   p->has_use = true;
