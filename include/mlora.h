@@ -119,7 +119,7 @@ MLORA_API size_t mlora_pool_bytes(int n_slots, int r_max, int K, int D);
 /* Creates a metadata object for steps of at most max_tokens tokens and max_slots_per_token
  * (J) adapter slots per token ("[RFC] ...", item 5: max_loras_per_request), for pools whose
  * r_max is at most r_max. Holds the sorted pair order, the segment table, per-pair scales
- * and the shrink workspace (max_tokens * J * r_max fp32, r_max rounded up to 8). */
+ * and the shrink workspace (16 * max_tokens * J * r_max fp32, r_max rounded up to 8). */
 MLORA_API mlora_status mlora_meta_create(int max_tokens, int max_slots_per_token, int r_max, mlora_meta_t* out);
 MLORA_API mlora_status mlora_meta_destroy(mlora_meta_t meta);
 

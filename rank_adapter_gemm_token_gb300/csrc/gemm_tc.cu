@@ -19,6 +19,7 @@
 #include <cooperative_groups.h>
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstdio>
 
 #include "internal.h"
@@ -191,9 +192,28 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
 // cluster (cluster rank = K split); each CTA stages its fp32 partial tile P[t][o] in its own
 // shared memory, and after a cluster barrier CTA r sums the partials of all CTAs for its share
 // of the tokens through distributed shared memory, always in rank order 0, 1, ... (so the
-// result is deterministic), and writes y with coalesced 16-byte stores.
+// result is deterministic), and writes the output with coalesced 16-byte stores.
+//
+// The shrink of the LoRA side path rides along ("Multi-LoRA Serving Explained", batched
+// serving: one large product shared by the batch plus each token's low-rank side path). The
+// step's active slots (those named by at least one token, ascending) contribute extra
+// 128-row blocks of A-operand rows: block b holds active slots b*(128/R) .. +128/R - 1, each
+// slot's R rows of A_pool fetched by its own TMA box, so each active adapter is read once and x
+// is shared with the base product. Their accumulators are v[t][a][q] = sum_i A_a[q][i] x[t][i]
+// for every token t and active slot a (written to vfull); the expand kernel then picks each
+// token's own slots.
+struct SkinnyShrink {
+  const int32_t* act_slot;   // active slots, ascending
+  const int32_t* n_act;      // device count of active slots
+  float* vfull;              // [T][vfull_ld] fp32, active slot a at columns a*R .. a*R + R - 1
+  int vfull_ld;
+  int R;                     // rows per slot in the A pool (multiple of 8, divides 128)
+  int n_ablk;                // A-row blocks in the grid (enough for every possible active slot)
+};
+
 constexpr int kSkinnyStages = 4;
 constexpr int kSkinnyABytes = BM * BK * 2;
+constexpr int kSkinnyMaxSplit = 8;
 
 __host__ __device__ constexpr int skinny_stage_bytes(int NT) { return kSkinnyABytes + NT * BK * 2; }
 __host__ __device__ constexpr int skinny_smem_bytes(int NT) {
@@ -202,8 +222,8 @@ __host__ __device__ constexpr int skinny_smem_bytes(int NT) {
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                        float* __restrict__ y, int T, int D, int K, int NT, int splitk, uint32_t tmem_cols,
-                        uint32_t* __restrict__ err) {
+                        const __grid_constant__ CUtensorMap tmap_a, float* __restrict__ y, int T, int D, int K,
+                        int NT, int splitk, uint32_t tmem_cols, uint32_t* __restrict__ err, SkinnyShrink sh) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,8 +237,17 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   cg::cluster_group cluster = cg::this_cluster();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int n_wblk = (D + BM - 1) / BM;
   const int oblk = blockIdx.x / splitk;
   const int ks = static_cast<int>(cluster.block_rank());
+  const bool a_blk = oblk >= n_wblk;                    // a block of active-slot A rows
+  const int spb = a_blk ? BM / sh.R : 0;                // slots per A block
+  const int a0 = a_blk ? (oblk - n_wblk) * spb : 0;     // first active slot of the block
+  int n_act = 0;
+  if (a_blk) {
+    n_act = *sh.n_act;
+    if (a0 >= n_act) return;                            // the whole cluster leaves together
+  }
   const int o0 = oblk * BM;
   const int num_kb = (K + BK - 1) / BK;
   const int kb0 = ks * num_kb / splitk, kb1 = (ks + 1) * num_kb / splitk;
@@ -231,7 +260,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
     ptx::mbar_init(acc_full, 1);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
-    ptx::tma_prefetch_desc(&tmap_w);
+    ptx::tma_prefetch_desc(a_blk ? &tmap_a : &tmap_w);
     ptx::tma_prefetch_desc(&tmap_x);
   }
   if (warp == 1) {
@@ -242,17 +271,29 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
+      // A rows of the block: one TMA box per active slot (R rows each) or one W box of 128 rows
+      int slot_row[BM / 8];
+      int n_box = 1;
+      if (a_blk) {
+        n_box = min(spb, n_act - a0);
+        for (int i = 0; i < n_box; ++i) slot_row[i] = sh.act_slot[a0 + i] * sh.R;
+      }
+      const uint32_t bytes = static_cast<uint32_t>(a_blk ? n_box * sh.R * BK * 2 + NT * BK * 2 : stage_bytes);
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) break;
         uint8_t* sa = smem + stage * stage_bytes;
-        ptx::mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(stage_bytes));
-        ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
+        ptx::mbar_arrive_expect_tx(&full[stage], bytes);
+        if (a_blk) {
+          for (int i = 0; i < n_box; ++i)
+            ptx::tma_load_2d(sa + i * sh.R * BK * 2, &tmap_a, &full[stage], kb * BK, slot_row[i]);
+        } else {
+          ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
+        }
         ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
         if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
       }
@@ -278,7 +319,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
       if (mma_ok) ptx::umma_commit(acc_full);
     }
   } else {
-    // TMEM lane = output feature o (warp w reads lanes 32*(w%4)..), columns = tokens
+    // TMEM lane = output row o (warp w reads lanes 32*(w%4)..), columns = tokens
     const int quarter = warp & 3;
     const int o = quarter * 32 + lane;
     if (ptx::mbar_wait(acc_full, 0, err)) {
@@ -291,37 +332,44 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
 #pragma unroll
         for (int i = 0; i < 32; ++i) part[(c + i) * BM + o] = __uint_as_float(r[i]);
       }
-    } else {
-      ok = false;
     }
   }
   ptx::tc_fence_before();
-  cluster.sync();                                     // every partial tile is in shared memory
+  ptx::cluster_sync_all();                            // every partial tile is in shared memory
 
-  // Reduction: CTA ks owns tokens [t0, t1); float4 over o, partials summed in rank order.
+  // CTA ks owns tokens [t0, t1): float4 over rows, partials summed in rank order.
   const int per = (T + splitk - 1) / splitk;
   const int t0 = ks * per, t1 = min(T, t0 + per);
-  for (int i = threadIdx.x; i < (t1 - t0) * (BM / 4); i += kGemmThreads) {
-    const int t = t0 + i / (BM / 4);
-    const int o4 = (i % (BM / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < splitk; ++r) {
-      const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    const int o = o0 + o4;
-    float* dst = y + static_cast<size_t>(t) * D + o;
-    if (o + 4 <= D && (D & 3) == 0) {
-      *reinterpret_cast<float4*>(dst) = acc;
+  const int rows = a_blk ? min(spb, n_act - a0) * sh.R : BM;
+  for (int w = threadIdx.x; w < (t1 - t0) * (BM / 4); w += kGemmThreads) {
+    const int t = t0 + w / (BM / 4);
+    const int o4 = (w % (BM / 4)) * 4;
+    if (o4 >= rows) continue;
+    float4 pv[kSkinnyMaxSplit];
+#pragma unroll
+    for (int r = 0; r < kSkinnyMaxSplit; ++r)
+      if (r < splitk) pv[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
+    float4 acc = pv[0];
+#pragma unroll
+    for (int r = 1; r < kSkinnyMaxSplit; ++r)
+      if (r < splitk) { acc.x += pv[r].x; acc.y += pv[r].y; acc.z += pv[r].z; acc.w += pv[r].w; }
+    if (a_blk) {
+      *reinterpret_cast<float4*>(sh.vfull + static_cast<size_t>(t) * sh.vfull_ld + a0 * sh.R + o4) = acc;
     } else {
-      if (o < D) dst[0] = acc.x;
-      if (o + 1 < D) dst[1] = acc.y;
-      if (o + 2 < D) dst[2] = acc.z;
-      if (o + 3 < D) dst[3] = acc.w;
+      const int o = o0 + o4;
+      float* dst = y + static_cast<size_t>(t) * D + o;
+      if (o + 4 <= D && (D & 3) == 0) {
+        *reinterpret_cast<float4*>(dst) = acc;
+      } else {
+        if (o < D) dst[0] = acc.x;
+        if (o + 1 < D) dst[1] = acc.y;
+        if (o + 2 < D) dst[2] = acc.z;
+        if (o + 3 < D) dst[3] = acc.w;
+      }
     }
   }
-  (void)ok;
-  cluster.sync();                                     // no CTA leaves while others read its tile
+  ptx::grid_dependents_launch();                      // the expand may start its set-up
+  ptx::cluster_sync_all();                            // no CTA leaves while others read its tile
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, tmem_cols);
@@ -385,15 +433,20 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
   return e;
 }
 
-cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
-                          int num_sms, cudaStream_t s) {
-  const int NT = (T + 15) / 16 * 16;
-  const int n_oblk = (D + BM - 1) / BM;
+int skinny_splitk(int n_oblk, int K, int num_sms) {
   const int num_kb = (K + BK - 1) / BK;
   int splitk = num_sms / n_oblk;
-  if (splitk > 8) splitk = 8;
+  if (splitk > kSkinnyMaxSplit) splitk = kSkinnyMaxSplit;
   if (splitk > num_kb) splitk = num_kb;
   if (splitk < 1) splitk = 1;
+  return splitk;
+}
+
+cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                          int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
+  const int NT = (T + 15) / 16 * 16;
+  const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
+  const int splitk = skinny_splitk(n_oblk, K, num_sms);
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(NT)) tmem_cols <<= 1;
   const int smem = skinny_smem_bytes(NT);
@@ -406,8 +459,13 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap mw, mx;
+  CUtensorMap mw, mx, ma;
   if (!make_tmap_bf16(&mw, W, D, K, BM, BK) || !make_tmap_bf16(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
+  if (sh.n_ablk > 0) {
+    if (!make_tmap_bf16(&ma, A_pool, S * sh.R, K, sh.R, BK)) return cudaErrorInvalidValue;
+  } else {
+    ma = mw;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_oblk * splitk, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
@@ -421,7 +479,8 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   note_launch_begin(kKindGemm, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, y, T, D, K, NT, splitk, tmem_cols, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, T, D, K, NT, splitk, tmem_cols,
+                                     err, sh);
   note_launch_end(kKindGemm, s);
   return e;
 }
@@ -431,12 +490,34 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                              uint32_t* err, int num_sms, cudaStream_t s) {
   if (T == 0 || D == 0) return cudaSuccess;
-  if (T <= 256) return launch_skinny(x, W, y, T, K, D, err, num_sms, s);
+  if (T <= kSkinnyMaxT) {
+    SkinnyShrink none{};
+    return launch_skinny(x, W, y, T, K, D, err, num_sms, nullptr, 0, none, s);
+  }
   // Largest N tile that still gives every SM a tile; small problems take N = 64.
   const int m_tiles = (T + BM - 1) / BM;
   if (m_tiles * ((D + 255) / 256) >= num_sms) return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, s);
   if (m_tiles * ((D + 127) / 128) >= num_sms) return launch_tc<128, 6>(x, W, y, T, K, D, err, num_sms, s);
   return launch_tc<64, 8>(x, W, y, T, K, D, err, num_sms, s);
+}
+
+}  // namespace mlora
+
+namespace mlora {
+
+bool skinny_shrink_fusable(int T, int J, int S, int R, int vfull_ld) {
+  if (T < 1 || T > kSkinnyMaxT || T > kVfullMaxTokens) return false;
+  if (R < 8 || R > BM || BM % R != 0) return false;
+  const int max_act = std::min(S, T * J);
+  return max_act * R <= vfull_ld;
+}
+
+cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float* y, const PoolView& pool,
+                                     const MetaView& m, uint32_t* err, int num_sms, cudaStream_t s) {
+  if (m.T == 0 || pool.D == 0) return cudaSuccess;
+  const int max_act = std::min(pool.S, m.n);
+  SkinnyShrink sh{m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R, (max_act * pool.R + BM - 1) / BM};
+  return launch_skinny(x, W, y, m.T, pool.K, pool.D, err, num_sms, pool.A, pool.S, sh, s);
 }
 
 }  // namespace mlora

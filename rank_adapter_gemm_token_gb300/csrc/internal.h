@@ -12,6 +12,7 @@ constexpr int kMaxRank = 256;       // r_max
 constexpr int kMaxJ = 8;            // adapter slots per token
 constexpr int kPairBlock = 16;      // pairs of one slot handled together by the shrink
 constexpr int kMetaThreads = 1024;
+constexpr int kMaxShrinkSplits = 16;   // K splits of the shrink (partial sums per split)
 
 // Device arrays of one adapter pool (one adapted linear).
 struct PoolView {
@@ -32,12 +33,22 @@ struct MetaView {
   int32_t* blk_slot;    // [n] pair-blocks of at most kPairBlock pairs of one slot
   int32_t* blk_start;   // [n]   start of the block inside order
   int32_t* blk_count;   // [n]   pairs in the block
-  int32_t* counts;      // [4] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none)
+  int32_t* counts;      // [8] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none),
+                        //     n_act (distinct slots with an active pair)
+  int32_t* pair_act;    // [n] index of the pair's slot among the active slots (-1: none)
+  int32_t* act_slot;    // [n] active slots in ascending order
   uint32_t* err;        // device error word (ptx::kErr* bits)
-  float* vpart;         // shrink output v: [n][R] fp32 (unscaled A x per pair)
+  float* vpart;         // shrink output: [n_splits][n][R] fp32 partial sums of A x per K split
+  float* vfull;         // small-batch shrink output: [T][act][R] fp32, row stride vfull_ld floats
+  int vfull_ld;
   int n;                // pairs of the current step (T * J)
   int T, J;
 };
+
+// Small batches fold the shrink into the skinny GEMM (v of every token against every active
+// slot, written to MetaView::vfull); the workspace covers these sizes.
+constexpr int kVfullMaxTokens = 256;
+constexpr int kVfullMaxAct = 512;
 
 // Kernel kinds for the launch counter and the optional per-kernel event trace.
 enum KernelKind : int { kKindMeta = 0, kKindGemm = 1, kKindShrink = 2, kKindExpand = 3, kKindSlot = 4, kNumKinds = 5 };
@@ -54,6 +65,20 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                              uint32_t* err, int num_sms, cudaStream_t s);
 
+constexpr int kSkinnyMaxT = 256;   // batches up to this size use the split-K skinny GEMM
+
+// Whether the skinny GEMM can compute the shrink alongside the base product for this step.
+bool skinny_shrink_fusable(int T, int J, int S, int R, int vfull_ld);
+// y = x W^T and vfull[t][a][q] = sum_i A_{act_slot[a]}[q][i] x[t][i] in one split-K tensor-core
+// kernel (T <= kSkinnyMaxT).
+cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float* y, const PoolView& pool,
+                                     const MetaView& m, uint32_t* err, int num_sms, cudaStream_t s);
+// y += sum_j s c B v with v from vfull; programmatic dependent launch after the fused GEMM.
+cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
+                                     cudaStream_t s);
+
+// K elements per shrink split and the number of splits for a pool of width R.
+void shrink_split(int K, int R, int* kc_len, int* n_ks);
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
                                cudaStream_t s);
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s);

@@ -8,10 +8,10 @@
 // -1 skipped, each weighted by its own scale, iterated inside one fused pass. "[vLLM] LoRA"
 // (secrett2633 blog), PEFTHelper: the slot factor is alpha/r, alpha/sqrt(r) under rsLoRA.
 //
-// Shrink works per pair-block (at most 16 pairs of one slot, from the sorted metadata): each
-// warp streams one row of A[slot] over the whole K range once with 16-byte loads, reusing each
-// vector for the pairs of the block, and writes the unscaled fp32 v[p][q]. Expand multiplies
-// v by the pair's scale times the slot factor. With one slot per token it works per pair-block and
+// Shrink works per pair-block (at most 16 pairs of one slot, from the sorted metadata) and K
+// split: each lane streams its share of A[slot] once with 16-byte loads, reusing each vector
+// for the pairs of the block, and writes unscaled fp32 partial sums per split. Expand adds the
+// splits in a fixed order and multiplies by the pair's scale times the slot factor. With one slot per token it works per pair-block and
 // 512-column range: B[slot] rows are read once per block (thread = output column, so both
 // the B rows and y are accessed coalesced) and each y element receives exactly one update.
 // With several slots per token it works per token, adding the slots in order j = 0..J-1.
@@ -23,7 +23,7 @@
 namespace mlora {
 namespace {
 
-constexpr int kShrinkThreads = 512;      // 16 warps; a warp owns one adapter row at a time
+constexpr int kShrinkThreads = 256;      // 8 warps; warp w owns adapter rows w, w + 8, ...
 constexpr int kExpandThreads = 256;      // one output column per thread, coalesced B rows and y
 constexpr int kExpandColsPerItem = 512;  // two columns per thread per item
 
@@ -51,25 +51,30 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4& b, const float* v) {
   return a;
 }
 
-// Item = one pair-block (at most 16 pairs of one slot). Warp w owns adapter rows w, w + 16, ...
-// and covers the whole K range: lane l reads 8-element vectors l, l + 32, ... of the row with
-// 16-byte loads (eight in flight per lane), reusing each vector for a group of 4 pairs from
-// registers; a warp shuffle then gives the final dot products, so v needs no cross-CTA sum.
-__global__ void __launch_bounds__(kShrinkThreads, 1)
-lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m) {
+// Item = (pair-block, K split). Warp w owns adapter rows w, w + 8, ... (RPW of them per group of
+// rows); lane l covers 8-element vectors l, l + 32, ... of the split. Each lane loads its A
+// vectors once (eight 16-byte loads in flight) and reuses them for every pair of the block, so
+// the dot products need only warp shuffles. The split's fp32 partial sums go to
+// vpart[split][p][q]; a consumer adds the splits in order 0, 1, ... . Items are spread over
+// every SM, and the kernel lets a dependent kernel (programmatic launch) start right away.
+template <int RPW>
+__global__ void __launch_bounds__(kShrinkThreads)
+lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, int kc_len, int n_ks) {
   constexpr int G = 4;                                        // pairs per register group
-  constexpr int U = 8;                                        // vector steps in flight per lane
+  constexpr int V = 8 / RPW;                                  // vectors per lane per row
+  ptx::grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_blocks = m.counts[2];
+  const int items = m.counts[2] * n_ks;
   const int K = pool.K, R = pool.R;
-  const int nvec = K / 8;
-  for (int b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / n_ks, ks = item - b * n_ks;
     const int slot = m.blk_slot[b];
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
-    for (int q = warp; q < rank; q += kShrinkThreads / 32) {
-      const uint4* arow = reinterpret_cast<const uint4*>(pool.A + (static_cast<size_t>(slot) * R + q) * K);
+    const int k0 = ks * kc_len;
+    const int nv = (min(K, k0 + kc_len) - k0) / 8;            // vectors in this split
+    for (int qg = warp; qg < rank; qg += 8 * RPW) {           // rows qg + 8 i, i < RPW
       for (int g0 = 0; g0 < cnt; g0 += G) {
         const int gc = min(G, cnt - g0);
         int pr[G];
@@ -77,47 +82,62 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m) {
 #pragma unroll
         for (int i = 0; i < G; ++i) {
           pr[i] = m.order[start + g0 + (i < gc ? i : 0)];
-          xv[i] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(pr[i] / m.J) * K);
+          xv[i] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(pr[i] / m.J) * K + k0);
         }
-        float acc[G];
+        float acc[RPW][G];
 #pragma unroll
-        for (int i = 0; i < G; ++i) acc[i] = 0.f;
-        int u = lane;
-        for (; u + 32 * (U - 1) < nvec; u += 32 * U) {
-          uint4 a[U];
+        for (int r = 0; r < RPW; ++r)
 #pragma unroll
-          for (int k = 0; k < U; ++k) a[k] = __ldg(arow + u + 32 * k);
+          for (int i = 0; i < G; ++i) acc[r][i] = 0.f;
+        for (int u0 = lane; u0 < nv; u0 += 32 * V) {
+          uint4 a[RPW][V];
+#pragma unroll
+          for (int r = 0; r < RPW; ++r) {
+            const int q = qg + 8 * r;
+            const uint4* arow = reinterpret_cast<const uint4*>(pool.A + (static_cast<size_t>(slot) * R + q) * K + k0);
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+              const int u = u0 + 32 * v;
+              a[r][v] = (q < rank && u < nv) ? __ldg(arow + u) : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             if (i < gc) {
-              float s = 0.f;
 #pragma unroll
-              for (int k = 0; k < U; ++k) s += dot8_bf16(a[k], __ldg(xv[i] + u + 32 * k));
-              acc[i] += s;
+              for (int v = 0; v < V; ++v) {
+                const int u = u0 + 32 * v;
+                if (u < nv) {
+                  const uint4 xx = __ldg(xv[i] + u);
+#pragma unroll
+                  for (int r = 0; r < RPW; ++r) acc[r][i] += dot8_bf16(a[r][v], xx);
+                }
+              }
             }
           }
         }
-        for (; u < nvec; u += 32) {
-          const uint4 a0 = __ldg(arow + u);
 #pragma unroll
-          for (int i = 0; i < G; ++i)
-            if (i < gc) acc[i] += dot8_bf16(a0, __ldg(xv[i] + u));
-        }
+        for (int r = 0; r < RPW; ++r) {
 #pragma unroll
-        for (int i = 0; i < G; ++i) {
-          float v = acc[i];
+          for (int i = 0; i < G; ++i) {
+            float v = acc[r][i];
 #pragma unroll
-          for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-          if (lane == 0 && i < gc) m.vpart[static_cast<size_t>(pr[i]) * R + q] = v;
+            for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+            const int q = qg + 8 * r;
+            if (lane == 0 && i < gc && q < rank) m.vpart[(static_cast<size_t>(ks) * m.n + pr[i]) * R + q] = v;
+          }
         }
       }
     }
   }
 }
 
-// v of pair p (unscaled shrink output) times coef, zero beyond the rank.
-__device__ __forceinline__ float pair_v(const MetaView& m, int R, int p, int q, int rank, float coef) {
-  return q < rank ? coef * m.vpart[static_cast<size_t>(p) * R + q] : 0.f;
+// v of pair p: the K-split partials added in order, times coef; zero beyond the rank.
+__device__ __forceinline__ float pair_v(const MetaView& m, int R, int n_ks, int p, int q, int rank, float coef) {
+  if (q >= rank) return 0.f;
+  float v = 0.f;
+  for (int ks = 0; ks < n_ks; ++ks) v += m.vpart[(static_cast<size_t>(ks) * m.n + p) * R + q];
+  return coef * v;
 }
 
 // J == 1: item = (pair-block, 512-column range). The block's scaled v rows sit in shared memory;
@@ -125,7 +145,7 @@ __device__ __forceinline__ float pair_v(const MetaView& m, int R, int p, int q, 
 // updates y[t][o] for every token of the block (consecutive o, coalesced). Each y element is
 // updated by exactly one pair, so the result is deterministic.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
   const int items = m.counts[2] * n_dchunk;
@@ -142,7 +162,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
     for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
       const int pi = i / rpad, q = i - pi * rpad;
       const int p = m.order[start + pi];
-      vs[pi][q] = pair_v(m, R, p, q, rank, c * m.pair_scale[p]);
+      vs[pi][q] = pair_v(m, R, n_ks, p, q, rank, c * m.pair_scale[p]);
       if (q == 0) tok[pi] = p;                      // J == 1: token index == pair index
     }
     __syncthreads();
@@ -168,7 +188,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
 // J > 1: item = (token, 512-column range); slots are added in order j = 0..J-1 so every output
 // is a fixed sequence of fp32 additions. Thread c owns column o: B rows and y coalesced.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk) {
   __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
@@ -190,7 +210,7 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
     __syncthreads();
     for (int i = threadIdx.x; i < J * R; i += kExpandThreads) {
       const int j = i / R, q = i - j * R;
-      vs[j][q] = ss[j] >= 0 ? pair_v(m, R, t * J + j, q, rs[j], cs[j]) : 0.f;
+      vs[j][q] = ss[j] >= 0 ? pair_v(m, R, n_ks, t * J + j, q, rs[j], cs[j]) : 0.f;
     }
     __syncthreads();
     for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
@@ -209,15 +229,150 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Expand after the small-batch fused GEMM, which leaves v of every token against every active
+// slot in vfull[t][a][q]. These kernels are programmatic dependents of that GEMM: everything
+// that does not depend on it (the step's metadata, the B rows, which are prefetched into L2) is
+// done before griddepcontrol.wait, and only v and y are touched after it.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// One slot per token: item = (pair-block, 512-column range), as in lora_expand_segment_kernel.
+__global__ void __launch_bounds__(kExpandThreads)
+lora_expand_vfull_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+  __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
+  __shared__ int tok[kPairBlock];
+  const int items = m.counts[2] * n_dchunk;
+  const int R = pool.R, D = pool.D;
+  bool waited = false;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = item / n_dchunk, dc = item - b * n_dchunk;
+    const int slot = m.blk_slot[b];
+    const int start = m.blk_start[b];
+    const int cnt = m.blk_count[b];
+    const int rank = pool.slot_rank[slot];
+    const float c = pool.slot_scale[slot];
+    const int rpad = (rank + 7) & ~7;
+    const int oa = dc * kExpandColsPerItem;
+    const int ob = min(D, oa + kExpandColsPerItem);
+    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads)
+      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(slot) * D + o) * R + u);
+    if (!waited) {
+      ptx::grid_dependency_wait();
+      waited = true;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
+      const int pi = i / rpad, q = i - pi * rpad;
+      const int p = m.order[start + pi];
+      vs[pi][q] = q < rank ? c * m.pair_scale[p] * m.vfull[static_cast<size_t>(p) * m.vfull_ld + m.pair_act[p] * R + q]
+                           : 0.f;
+      if (q == 0) tok[pi] = p;
+    }
+    __syncthreads();
+    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads) {
+      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
+      float d[kPairBlock];
+#pragma unroll
+      for (int i = 0; i < kPairBlock; ++i) d[i] = 0.f;
+      for (int u = 0; u < rpad / 8; ++u) {
+        const uint4 bv = __ldg(brow + u);
+#pragma unroll
+        for (int i = 0; i < kPairBlock; ++i)
+          if (i < cnt) d[i] += dot8_bf16_f32(bv, &vs[i][8 * u]);
+      }
+#pragma unroll
+      for (int i = 0; i < kPairBlock; ++i)
+        if (i < cnt) y[static_cast<size_t>(tok[i]) * D + o] += d[i];
+    }
+  }
+  if (!waited) ptx::grid_dependency_wait();
+}
+
+// Several slots per token: item = (token, 512-column range), slots added in order j = 0..J-1.
+__global__ void __launch_bounds__(kExpandThreads)
+lora_expand_vfull_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
+  __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
+  __shared__ float cs[kMaxJ];
+  __shared__ int ss[kMaxJ], rs[kMaxJ], as[kMaxJ];
+  const int J = m.J, R = pool.R, D = pool.D;
+  const int items = m.T * n_dchunk;
+  bool waited = false;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int t = item / n_dchunk, dc = item - t * n_dchunk;
+    bool any = false;
+    for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0;
+    if (!any) continue;                                // uniform across the block
+    __syncthreads();
+    if (threadIdx.x < J) {
+      const int p = t * J + threadIdx.x;
+      const int s = m.pair_slot[p];
+      ss[threadIdx.x] = s;
+      rs[threadIdx.x] = s >= 0 ? pool.slot_rank[s] : 0;
+      cs[threadIdx.x] = s >= 0 ? m.pair_scale[p] * pool.slot_scale[s] : 0.f;
+      as[threadIdx.x] = m.pair_act[p];
+    }
+    __syncthreads();
+    const int oa = dc * kExpandColsPerItem;
+    const int ob = min(D, oa + kExpandColsPerItem);
+    for (int j = 0; j < J; ++j)
+      if (ss[j] >= 0)
+        for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads)
+          for (int u = 0; u < rs[j]; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(ss[j]) * D + o) * R + u);
+    if (!waited) {
+      ptx::grid_dependency_wait();
+      waited = true;
+    }
+    for (int i = threadIdx.x; i < J * R; i += kExpandThreads) {
+      const int j = i / R, q = i - j * R;
+      vs[j][q] = (ss[j] >= 0 && q < rs[j])
+                     ? cs[j] * m.vfull[static_cast<size_t>(t) * m.vfull_ld + as[j] * R + q]
+                     : 0.f;
+    }
+    __syncthreads();
+    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads) {
+      float acc = y[static_cast<size_t>(t) * D + o];
+      for (int j = 0; j < J; ++j) {
+        const int s = ss[j];
+        if (s < 0) continue;
+        const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(s) * D + o) * R);
+        float d = 0.f;
+        for (int u = 0; u < (rs[j] + 7) / 8; ++u) d += dot8_bf16_f32(__ldg(brow + u), &vs[j][8 * u]);
+        acc += d;
+      }
+      y[static_cast<size_t>(t) * D + o] = acc;
+    }
+  }
+  if (!waited) ptx::grid_dependency_wait();
+}
+
 }  // namespace
+
+int shrink_rows_per_warp(int R) { return R <= 8 ? 1 : R <= 16 ? 2 : R <= 32 ? 4 : 8; }
+
+void shrink_split(int K, int R, int* kc_len, int* n_ks) {
+  int kc = 256 * (8 / shrink_rows_per_warp(R));             // eight A vectors per lane
+  if ((K + kc - 1) / kc > kMaxShrinkSplits) kc = ((K + kMaxShrinkSplits - 1) / kMaxShrinkSplits + 255) / 256 * 256;
+  *kc_len = kc;
+  *n_ks = (K + kc - 1) / kc;
+}
 
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
                                cudaStream_t s) {
   if (m.n == 0) return cudaSuccess;
-  int grid = num_sms * 2;                                // blocks beyond the pair-block count exit
-  if (grid > m.n) grid = m.n;
+  int kc, n_ks;
+  shrink_split(pool.K, pool.R, &kc, &n_ks);
+  const int max_items = m.n * n_ks;                     // pair-blocks <= pairs
+  int grid = num_sms * 2;
+  if (grid > max_items) grid = max_items;
   note_launch_begin(kKindShrink, s);
-  lora_shrink_kernel<<<grid, kShrinkThreads, 0, s>>>(x, pool, m);
+  switch (shrink_rows_per_warp(pool.R)) {
+    case 1: lora_shrink_kernel<1><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
+    case 2: lora_shrink_kernel<2><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
+    case 4: lora_shrink_kernel<4><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
+    default: lora_shrink_kernel<8><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
+  }
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindShrink, s);
   return e;
@@ -225,16 +380,41 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
 
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s) {
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
+  int kc, n_ks;
+  shrink_split(pool.K, pool.R, &kc, &n_ks);
   const int n_dchunk = (pool.D + kExpandColsPerItem - 1) / kExpandColsPerItem;
   const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
   int grid = num_sms * 8;
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindExpand, s);
   if (m.J == 1)
-    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_dchunk);
+    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk);
   else
-    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_dchunk);
+    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk);
   cudaError_t e = cudaGetLastError();
+  note_launch_end(kKindExpand, s);
+  return e;
+}
+
+cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
+                                     cudaStream_t s) {
+  if (m.n == 0 || pool.D == 0) return cudaSuccess;
+  const int n_dchunk = (pool.D + kExpandColsPerItem - 1) / kExpandColsPerItem;
+  const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
+  int grid = num_sms * 8;
+  if (grid > max_items) grid = max_items;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kExpandThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launch_begin(kKindExpand, s);
+  cudaError_t e = (m.J == 1) ? cudaLaunchKernelEx(&cfg, lora_expand_vfull_segment_kernel, y, pool, m, n_dchunk)
+                             : cudaLaunchKernelEx(&cfg, lora_expand_vfull_token_kernel, y, pool, m, n_dchunk);
   note_launch_end(kKindExpand, s);
   return e;
 }

@@ -59,7 +59,8 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   int* hist = smem;                          // [nb] pairs per bin
   int* cursor = hist + nb;                   // [nb] next free position of each bin
   int* chunk_tot = cursor + nb;              // [nb] pairs per bin in the current chunk
-  uint16_t* wcnt = reinterpret_cast<uint16_t*>(chunk_tot + nb);   // [32][nb]
+  int* actidx = chunk_tot + nb;              // [nb] index among the active slots (-1: none)
+  uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
 
@@ -101,12 +102,18 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   }
   int ph, pf, pk;
   block_exclusive_scan3(h, f, k, ph, pf, pk, warp_sums);
+  const int has_sentinel = hist[0] > 0;
   for (int b = b0; b < b1; ++b) {
     const int c = hist[b];
     cursor[b] = ph;
+    actidx[b] = -1;
     if (c > 0) {
       m.seg_slot[pf] = b - 1;
       m.seg_off[pf] = ph;
+      if (b > 0) {
+        actidx[b] = pf - has_sentinel;
+        m.act_slot[pf - has_sentinel] = b - 1;
+      }
       ++pf;
       if (b > 0) {
         for (int i = 0; i * kPairBlock < c; ++i, ++pk) {
@@ -123,6 +130,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     m.counts[0] = pf;
     m.counts[1] = n - hist[0];
     m.counts[2] = pk;
+    m.counts[4] = pf - has_sentinel;
   }
   __syncthreads();
 
@@ -148,7 +156,10 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
       chunk_tot[b] = run;
     }
     __syncthreads();
-    if (valid) m.order[cursor[bin] + wcnt[warp * nb + bin] + rank_in_warp] = p;
+    if (valid) {
+      m.order[cursor[bin] + wcnt[warp * nb + bin] + rank_in_warp] = p;
+      m.pair_act[p] = actidx[bin];
+    }
     __syncthreads();
     for (int b = tid; b < nb; b += kMetaThreads) cursor[b] += chunk_tot[b];
     __syncthreads();
@@ -165,11 +176,11 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
                               const int32_t* slot_rank, const MetaView& m, cudaStream_t s) {
   const int nb = S + 1;
-  const size_t smem = static_cast<size_t>(nb) * (3 * sizeof(int) + 32 * sizeof(uint16_t));
+  const size_t smem = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>((kMaxSlots + 1) * (3 * sizeof(int) + 32 * sizeof(uint16_t))));
+                                         static_cast<int>((kMaxSlots + 1) * (4 * sizeof(int) + 32 * sizeof(uint16_t))));
     if (e != cudaSuccess) return e;
     configured = true;
   }

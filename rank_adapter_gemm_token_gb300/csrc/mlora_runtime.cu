@@ -9,6 +9,7 @@
 //   "LoRA Serving" (vLLM learning book ch. 09-04), section 4.1: activating an adapter copies
 //   its weights into a GPU slot; failure-injection list of section 13 (out-of-range slot,
 //   incompatible rank, reload of a slot in use, cancelling a load).
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -148,15 +149,18 @@ struct mlora_meta {
   int32_t *order = nullptr, *seg_slot = nullptr, *seg_off = nullptr, *pair_slot = nullptr;
   float* pair_scale = nullptr;
   int32_t *blk_slot = nullptr, *blk_start = nullptr, *blk_count = nullptr, *counts = nullptr;
+  int32_t *pair_act = nullptr, *act_slot = nullptr;
   uint32_t* err = nullptr;
   float* vpart = nullptr;
+  float* vfull = nullptr;
+  int vfull_ld = 0;
   int T = 0, J = 1, S = -1;
   bool built = false;
   cudaEvent_t done = nullptr;
 
   MetaView view() const {
-    return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count,
-                    counts, err, vpart, T * J, T, J};
+    return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count, counts,
+                    pair_act, act_slot, err, vpart, vfull, vfull_ld, T * J, T, J};
   }
 };
 
@@ -374,11 +378,17 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->blk_slot), n * 4);
   alloc(reinterpret_cast<void**>(&m->blk_start), n * 4);
   alloc(reinterpret_cast<void**>(&m->blk_count), n * 4);
-  alloc(reinterpret_cast<void**>(&m->counts), 4 * 4);
+  alloc(reinterpret_cast<void**>(&m->counts), 8 * 4);
+  alloc(reinterpret_cast<void**>(&m->pair_act), n * 4);
+  alloc(reinterpret_cast<void**>(&m->act_slot), (n + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->err), 4);
-  alloc(reinterpret_cast<void**>(&m->vpart), n * m->R_max * 4);
+  alloc(reinterpret_cast<void**>(&m->vpart), static_cast<size_t>(kMaxShrinkSplits) * n * m->R_max * 4);
+  // small-batch shrink output: v of every token (up to 256) against every active slot
+  const int vt = std::min(max_tokens, kVfullMaxTokens);
+  m->vfull_ld = std::min(m->n_max, kVfullMaxAct) * m->R_max;
+  alloc(reinterpret_cast<void**>(&m->vfull), static_cast<size_t>(vt) * m->vfull_ld * 4);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 4);
-  if (e == cudaSuccess) e = cudaMemset(m->counts, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(m->counts, 0, 32);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -408,6 +418,9 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->counts);
   cudaFree(m->err);
   cudaFree(m->vpart);
+  cudaFree(m->vfull);
+  cudaFree(m->pair_act);
+  cudaFree(m->act_slot);
   delete m;
   return MLORA_OK;
 }
@@ -439,9 +452,9 @@ mlora_status mlora_meta_status(mlora_meta_t m) {
   if (!m) return fail(MLORA_ERR_INVALID_ARG, "meta is NULL");
   MLORA_CUDA(cudaEventSynchronize(m->done), "meta sync");
   uint32_t err = 0, gerr = 0;
-  int32_t counts[4] = {0, 0, 0, 0};
+  int32_t counts[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   MLORA_CUDA(cudaMemcpy(&err, m->err, 4, cudaMemcpyDeviceToHost), "read meta error word");
-  MLORA_CUDA(cudaMemcpy(counts, m->counts, 16, cudaMemcpyDeviceToHost), "read meta counts");
+  MLORA_CUDA(cudaMemcpy(counts, m->counts, 32, cudaMemcpyDeviceToHost), "read meta counts");
   DeviceState* ds = nullptr;
   if (mlora_status st = device_state(&ds)) return st;
   MLORA_CUDA(cudaMemcpy(&gerr, ds->err, 4, cudaMemcpyDeviceToHost), "read device error word");
@@ -463,8 +476,8 @@ mlora_status mlora_meta_read(mlora_meta_t m, int32_t* order, int32_t* seg_slot, 
   if (!m) return fail(MLORA_ERR_INVALID_ARG, "meta is NULL");
   if (!m->built) return fail(MLORA_ERR_INVALID_ARG, "metadata has not been built");
   MLORA_CUDA(cudaEventSynchronize(m->done), "meta sync");
-  int32_t counts[4];
-  MLORA_CUDA(cudaMemcpy(counts, m->counts, 16, cudaMemcpyDeviceToHost), "read counts");
+  int32_t counts[8];
+  MLORA_CUDA(cudaMemcpy(counts, m->counts, 32, cudaMemcpyDeviceToHost), "read counts");
   const size_t n = static_cast<size_t>(m->T) * m->J;
   if (order && n) MLORA_CUDA(cudaMemcpy(order, m->order, n * 4, cudaMemcpyDeviceToHost), "read order");
   if (seg_slot && counts[0])
@@ -545,12 +558,21 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   if (mlora_status st = device_state(&ds)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
-  cudaError_t e = launch_base_gemm(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "base GEMM launch");
   const MetaView mv = m->view();
   const PoolView pv = p->view();
-  if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "shrink launch");
-  if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
+  cudaError_t e = cudaSuccess;
+  if (skinny_shrink_fusable(m->T, m->J, p->S, p->R, m->vfull_ld)) {
+    // small batch: one split-K tensor-core kernel for the base product and the shrink of every
+    // active slot, then the expand as its programmatic dependent
+    if ((e = launch_gemm_shrink_fused(x, W, y, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "fused GEMM launch");
+    if ((e = launch_lora_expand_vfull(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
+  } else {
+    if ((e = launch_base_gemm(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "base GEMM launch");
+    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "shrink launch");
+    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
+  }
   MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
   MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
   p->has_use = true;

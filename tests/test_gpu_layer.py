@@ -14,18 +14,34 @@ from tests.harness import DeviceWorkload, assert_close, errors, oracle_rows, sam
 pytestmark = pytest.mark.gpu
 
 
+def _sentinel_run(dw, dl):
+    """The same layer call with every slot set to -1 (same shapes, pool and grid)."""
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer
+    meta = layer.StepMeta(dw.wl.T, dw.wl.J, dw.wl.r_max)
+    meta.build(torch.full_like(dw.token_slots, -1), None, dl.pool)
+    out = layer.linear(dl.pool, meta, dw.x[dl.lin.x_id], dl.W).cpu().numpy()
+    meta.close()
+    return out
+
+
 def _check_linear(wl, dw, dl, rows=None, check_delta=True):
     from rank_adapter_gemm_token_gb300 import layer
     y = dl.y.cpu().numpy()
     ref = oracle_rows(wl, dl.lin, rows=rows)
     ysel = y if rows is None else y[rows]
     assert_close(ysel, ref, f"{wl.name}/{dl.lin.name}")
-    base_dev = layer.base_gemm(dw.x[dl.lin.x_id], dl.W).cpu().numpy()
+    base_dev = _sentinel_run(dw, dl)
     bsel = base_dev if rows is None else base_dev[rows]
-    # rows with no active slot equal the base product exactly
+    # rows with no active slot equal the base product of the same call exactly
     slots = wl.token_slots if rows is None else wl.token_slots[rows]
     idle = np.all(slots < 0, axis=1)
     assert np.array_equal(ysel[idle], bsel[idle]), "sentinel rows differ from the base product"
+    # ... and the standalone base GEMM up to fp32 summation order
+    gemm = layer.base_gemm(dw.x[dl.lin.x_id], dl.W).cpu().numpy()
+    gsel = gemm if rows is None else gemm[rows]
+    rel, _ = errors(bsel, gsel.astype(np.float64))
+    assert rel < 1e-5, f"base product differs from the standalone GEMM: {rel:.2e}"
     if check_delta and (~idle).any():
         base_ref = oracle.linear(wl.xs[dl.lin.x_id], dl.lin.W, np.full((wl.T, 1), -1), {}, wl.n_slots, rows=rows)
         rel, _ = errors(ysel[~idle] - bsel[~idle], ref[~idle] - base_ref[~idle])
@@ -147,8 +163,7 @@ def test_zero_scale_and_linearity_on_gpu(cuda_device):
         dw.scales = torch.full((wl.T, wl.J), s, dtype=torch.float32, device="cuda")
         dw.run()
         outs[s] = dw.linears[0].y.cpu().numpy().astype(np.float64)
-    from rank_adapter_gemm_token_gb300 import layer
-    base = layer.base_gemm(dw.x[0], dw.linears[0].W).cpu().numpy()
+    base = _sentinel_run(dw, dw.linears[0])
     assert np.array_equal(outs[0.0], base)                  # zero scale adds exact zeros
     rel, _ = errors(outs[0.5] - base, 0.5 * (outs[1.0] - base))
     assert rel < 1e-6
