@@ -167,6 +167,30 @@ MLORA_API mlora_status mlora_base_gemm(const mlora_bf16* x, const mlora_bf16* W,
 MLORA_API mlora_status mlora_lora_shrink(mlora_pool_t pool, mlora_meta_t meta, const mlora_bf16* x, void* stream);
 MLORA_API mlora_status mlora_lora_expand(mlora_pool_t pool, mlora_meta_t meta, float* y, void* stream);
 
+/* Allocation-free LoRA side path (no counterpart on the pages: an addition for callers that
+ * cannot allocate device memory, such as a serving engine that has handed all free device
+ * memory to its KV cache at start-up, so a later cudaMalloc fails, or code on a
+ * latency-critical path that cannot accept the implicit device synchronisation of
+ * cudaMalloc/cudaFree). It needs no pool or metadata object:
+ *   y[t, :] += sum_j s[t,j] * slot_scale[slot] * B_slot (A_slot x[t, :])  for slot = token_slots[t*J + j],
+ * over caller-owned device buffers laid out as a pool is (A_pool [n_slots, r_pad, K],
+ * B_pool [n_slots, D, r_pad] bf16, zero beyond each slot's rank; slot_scale [n_slots] fp32;
+ * slot_rank [n_slots] int32, 0 = empty). scales may be NULL (s = 1). A token slot outside
+ * [0, n_slots) or naming an empty slot adds nothing. y must already hold the base product.
+ * Its only workspace is a fixed array compiled into the library (4 MiB, held by every GPU
+ * that loads it until the process exits), so T * J * r_pad must not exceed 1,048,576
+ * (else MLORA_ERR_TOO_MANY_TOKENS, nothing launched). It calls no cudaMalloc, cudaFree or
+ * other allocating routine. The first call on each device looks up the workspace's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture. All calls share the workspace: calls that overlap on the GPU (different
+ * streams, devices aside) race and must be ordered by the caller. Nothing carries over
+ * between calls: every workspace value read was written earlier in the same call. */
+MLORA_API mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, const int32_t* token_slots,
+                                                const float* scales, int T, int J, const mlora_bf16* A_pool,
+                                                const mlora_bf16* B_pool, const float* slot_scale,
+                                                const int32_t* slot_rank, int n_slots, int r_pad, int K, int D,
+                                                void* stream);
+
 /* ------------------------------------------------------------------ diagnostics ------ */
 
 MLORA_API const char* mlora_status_string(mlora_status status);

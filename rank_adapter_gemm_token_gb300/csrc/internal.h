@@ -53,6 +53,10 @@ constexpr int kVfullMaxAct = 512;
 // Kernel kinds for the launch counter and the optional per-kernel event trace.
 enum KernelKind : int { kKindMeta = 0, kKindGemm = 1, kKindShrink = 2, kKindExpand = 3, kKindSlot = 4, kNumKinds = 5 };
 
+// Records the thread's last-error message and returns the status (mlora_runtime.cu).
+int report_error(int status, const char* message);
+int report_cuda_error(cudaError_t e, const char* what);
+
 // Launch counter + tracing hooks (mlora_runtime.cu).
 void note_launch_begin(int kind, cudaStream_t s);
 void note_launch_end(int kind, cudaStream_t s);

@@ -105,6 +105,9 @@ __global__ void set_slot_kernel(float* slot_scale, int32_t* slot_rank, int slot,
 
 namespace mlora {
 
+int report_error(int status, const char* message) { return fail(status, "%s", message); }
+int report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
 void note_launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!g_trace.on) return;

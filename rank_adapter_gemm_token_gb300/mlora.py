@@ -34,6 +34,7 @@ EXPORTS = (
     "mlora_meta_status", "mlora_meta_read", "mlora_linear", "mlora_base_gemm", "mlora_lora_shrink",
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
+    "mlora_lora_apply_noalloc",
 )
 
 
@@ -81,6 +82,7 @@ def load(path: str | None = None):
             "mlora_trace_enable": [i32],
             "mlora_trace_disable": [],
             "mlora_trace_read": [i32, vp, vp],
+            "mlora_lora_apply_noalloc": [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -215,6 +217,14 @@ def mlora_lora_shrink(pool: int, meta: int, x, stream=None) -> None:
 
 def mlora_lora_expand(pool: int, meta: int, y, stream=None) -> None:
     _check(load().mlora_lora_expand(pool, meta, _ptr(y), _stream(stream)), "mlora_lora_expand")
+
+
+def mlora_lora_apply_noalloc(x, y, token_slots, scales, T: int, J: int, A_pool, B_pool, slot_scale, slot_rank,
+                             n_slots: int, r_pad: int, K: int, D: int, stream=None) -> None:
+    """y += the LoRA side path, using only the caller's buffers and the library's built-in workspace."""
+    _check(load().mlora_lora_apply_noalloc(_ptr(x), _ptr(y), _ptr(token_slots), _ptr(scales), T, J, _ptr(A_pool),
+                                           _ptr(B_pool), _ptr(slot_scale), _ptr(slot_rank), n_slots, r_pad, K, D,
+                                           _stream(stream)), "mlora_lora_apply_noalloc")
 
 
 # ------------------------------------------------------------------------- diagnostics
