@@ -49,6 +49,21 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate_over_ranks(ms_local: float, tokens_per_rank: int) -> tuple:
+    """Whole-job timing: the slowest rank's ms per step and tokens/s over all ranks (each rank
+    runs its own replica of the workload, so the work per rank is fixed: weak scaling)."""
+    import torch
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    ms = float(ms_local)
+    if ws > 1:
+        dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, ws * tokens_per_rank / (ms / 1000.0)
+
+
 # ------------------------------------------------------------------------------ workload
 def make_workload(name: str):
     import synth
@@ -58,6 +73,8 @@ def make_workload(name: str):
         return synth.compose()
     if name == "tiny":
         return synth.tiny()
+    if name == "prefill":
+        return synth.prefill()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -77,25 +94,35 @@ def workload_config(wl, name: str) -> dict:
 
 
 def algorithmic_bytes(wl) -> dict:
-    """Bytes each kernel kind must move per step (unique data, counted once):
-    base GEMM: W + x + y write (fp32); shrink: A rows of the distinct active slots (true rank)
-    + x rows of active tokens + v write; expand: B rows of the distinct active slots (true rank,
-    padded to 8) + y read-modify-write of rows with an active slot + v read.
+    """Bytes each kernel kind must move per step (unique data, each counted once), by path.
+
+    Small batches (T <= 256: one split-K tensor-core kernel computes the base product and the
+    shrink of every active slot): base_gemm = W + x + y write (fp32) + A rows of the active slots
+    (R rows each, the pool's padded rank) + v write (T x active slots x R, fp32); expand = B rows
+    of the active slots at the true rank padded to 8 + read and write of y rows with an active
+    slot + v reads of the active pairs.
+    Larger batches: base_gemm = W + x + y; shrink = A rows at the true rank + x rows of active
+    tokens + v partial writes; expand = B rows + y read-modify-write + v reads.
     Flops: 2*T*K*D per linear for the base product."""
     slots = wl.token_slots
     active = slots >= 0
     act_rows = int(np.any(active, axis=1).sum())
     pairs = int(active.sum())
     distinct = sorted(set(int(s) for s in slots[active]))
-    out = {"base_gemm": 0, "shrink": 0, "expand": 0, "base_flops": 0, "meta": 0}
+    R = (wl.r_max + 7) // 8 * 8
+    small = wl.T <= 256
+    out = {"base_gemm": 0, "shrink": 0, "expand": 0, "base_flops": 0, "meta": wl.T * wl.J * 4 * 6}
     for l in wl.linears:
         out["base_gemm"] += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
         out["base_flops"] += 2 * wl.T * l.K * l.D
         ra = sum(l.adapters[s].rank for s in distinct)
         rb = sum((l.adapters[s].rank + 7) // 8 * 8 for s in distinct)
-        out["shrink"] += ra * l.K * 2 + act_rows * l.K * 2 + pairs * wl.r_max * 4
-        out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * wl.r_max * 4
-    out["meta"] = wl.T * wl.J * 4 * 6
+        if small:
+            out["base_gemm"] += len(distinct) * R * l.K * 2 + wl.T * len(distinct) * R * 4
+            out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
+        else:
+            out["shrink"] += ra * l.K * 2 + act_rows * l.K * 2 + pairs * R * 4
+            out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
     return out
 
 
@@ -299,12 +326,7 @@ def run_ours(args):
     launches = mlora.mlora_launch_count() - launches0
     clock_info = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = float(np.mean(step_ms))
-    if ws > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * wl.T / (ms / 1000.0)
+    ms, value = aggregate_over_ranks(float(np.mean(step_ms)), wl.T)
 
     # ---- per-kernel durations: the same K steps again with the library's event trace
     trace_steps = min(args.steps, 100)
@@ -340,7 +362,7 @@ def run_ours(args):
         e_end.record(stream)
         e_end.synchronize()
         e2e_ms.append(e_start.elapsed_time(e_end))
-    e2e_value = ws * wl.T / (float(np.mean(e2e_ms)) / 1000.0)
+    _, e2e_value = aggregate_over_ranks(float(np.mean(e2e_ms)), wl.T)
     dw.meta.status()
 
     if rank != 0:
@@ -420,7 +442,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "tiny"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -1,0 +1,52 @@
+"""The N > 1 host path of the benchmark on CPU: two gloo ranks, each with its own replica,
+agree on the slowest rank's step time and report whole-job tokens/s (weak scaling)."""
+import os
+import socket
+
+import pytest
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms_local = [1.5, 2.25][rank]
+    ms, value = bench.aggregate_over_ranks(ms_local, 256)
+    out.put((rank, ms, value))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_rank():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, ms, value in res:
+        assert ms == 2.25
+        assert value == pytest.approx(2 * 256 / 2.25e-3)
+
+
+def test_reference_arm_on_a_non_zero_rank_does_nothing(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+
+    class A:
+        workload, steps, warmup = "tiny", 1, 3
+    assert bench.run_reference(A()) == 0
+    assert capsys.readouterr().out == ""
