@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cstdio>
 
+#include "expand_vfull.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -203,6 +204,9 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
 // for every token t and active slot a (written to vfull); the expand kernel then picks each
 // token's own slots.
 struct SkinnyShrink {
+  PoolView pool;             // expand operands: B rows of the slots prefetched into L2 meanwhile
+  MetaView meta;
+  int n_dchunk;              // column ranges of the expand that follows (0: no prefetch)
   const int32_t* act_slot;   // active slots, ascending
   const int32_t* n_act;      // device count of active slots
   float* vfull;              // [T][vfull_ld] fp32, active slot a at columns a*R .. a*R + R - 1
@@ -243,15 +247,13 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   const bool a_blk = oblk >= n_wblk;                    // a block of active-slot A rows
   const int spb = a_blk ? BM / sh.R : 0;                // slots per A block
   const int a0 = a_blk ? (oblk - n_wblk) * spb : 0;     // first active slot of the block
-  int n_act = 0;
-  if (a_blk) {
-    n_act = *sh.n_act;
-    if (a0 >= n_act) return;                            // the whole cluster leaves together
-  }
   const int o0 = oblk * BM;
   const int num_kb = (K + BK - 1) / BK;
   const int kb0 = ks * num_kb / splitk, kb1 = (ks + 1) * num_kb / splitk;
 
+  // Set-up that depends on no earlier kernel (programmatic dependent launch lets it overlap the
+  // previous kernel's tail): barriers, TMEM, descriptor prefetch, and this CTA's W range
+  // prefetched into L2 (a hint only; the operand loads below come after the dependency wait).
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSkinnyStages; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -263,6 +265,8 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
     ptx::tma_prefetch_desc(a_blk ? &tmap_a : &tmap_w);
     ptx::tma_prefetch_desc(&tmap_x);
   }
+  if (warp == 2 && !a_blk)
+    for (int kb = kb0 + lane; kb < kb1; kb += 32) ptx::tma_prefetch_l2_2d(&tmap_w, kb * BK, o0);
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, tmem_cols);
     ptx::tmem_relinquish();
@@ -272,7 +276,19 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  ptx::grid_dependency_wait();                          // earlier kernels' writes are visible
+  ptx::grid_dependents_launch();                        // the next kernel may start its set-up
+  int n_act = 0;
+  bool idle = false;                                    // an A block with no active slot
+  if (a_blk) {
+    n_act = *sh.n_act;
+    idle = a0 >= n_act;                                 // uniform across the cluster
+  }
+  const int n_exp_items = sh.n_dchunk ? (sh.meta.J == 1 ? sh.meta.counts[2] : sh.meta.T) * sh.n_dchunk : 0;
+
+  if (idle) {
+    // nothing to multiply: only the expand phase below (if any)
+  } else if (warp == 0) {
     if (lane == 0) {
       // A rows of the block: one TMA box per active slot (R rows each) or one W box of 128 rows
       int slot_row[BM / 8];
@@ -319,57 +335,81 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
       if (mma_ok) ptx::umma_commit(acc_full);
     }
   } else {
+    // While the main loop runs, bring into L2 the B rows the expand kernel will read (a share
+    // of its items per block).
+    for (int item = blockIdx.x; item < n_exp_items; item += gridDim.x)
+      expand_vfull_prefetch(sh.pool, sh.meta, item, sh.n_dchunk, threadIdx.x - 64, kGemmThreads - 64);
     // TMEM lane = output row o (warp w reads lanes 32*(w%4)..), columns = tokens
     const int quarter = warp & 3;
     const int o = quarter * 32 + lane;
     if (ptx::mbar_wait(acc_full, 0, err)) {
       ptx::tc_fence_after();
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < NT; c += 32) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c), r);
+      for (int c = 0; c < NT; c += 64) {                // two loads in flight per wait
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c), r0);
+        if (c + 32 < NT) ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c + 32), r1);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) part[(c + i) * BM + o] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) part[(c + i) * BM + o] = __uint_as_float(r0[i]);
+        if (c + 32 < NT) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) part[(c + 32 + i) * BM + o] = __uint_as_float(r1[i]);
+        }
       }
     }
   }
-  ptx::tc_fence_before();
-  ptx::cluster_sync_all();                            // every partial tile is in shared memory
+  if (!idle) {
+    ptx::tc_fence_before();
+    ptx::cluster_sync_all();                            // every partial tile is in shared memory
 
-  // CTA ks owns tokens [t0, t1): float4 over rows, partials summed in rank order.
-  const int per = (T + splitk - 1) / splitk;
-  const int t0 = ks * per, t1 = min(T, t0 + per);
-  const int rows = a_blk ? min(spb, n_act - a0) * sh.R : BM;
-  for (int w = threadIdx.x; w < (t1 - t0) * (BM / 4); w += kGemmThreads) {
-    const int t = t0 + w / (BM / 4);
-    const int o4 = (w % (BM / 4)) * 4;
-    if (o4 >= rows) continue;
-    float4 pv[kSkinnyMaxSplit];
-#pragma unroll
-    for (int r = 0; r < kSkinnyMaxSplit; ++r)
-      if (r < splitk) pv[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
-    float4 acc = pv[0];
-#pragma unroll
-    for (int r = 1; r < kSkinnyMaxSplit; ++r)
-      if (r < splitk) { acc.x += pv[r].x; acc.y += pv[r].y; acc.z += pv[r].z; acc.w += pv[r].w; }
-    if (a_blk) {
-      *reinterpret_cast<float4*>(sh.vfull + static_cast<size_t>(t) * sh.vfull_ld + a0 * sh.R + o4) = acc;
-    } else {
-      const int o = o0 + o4;
-      float* dst = y + static_cast<size_t>(t) * D + o;
-      if (o + 4 <= D && (D & 3) == 0) {
-        *reinterpret_cast<float4*>(dst) = acc;
-      } else {
-        if (o < D) dst[0] = acc.x;
-        if (o + 1 < D) dst[1] = acc.y;
-        if (o + 2 < D) dst[2] = acc.z;
-        if (o + 3 < D) dst[3] = acc.w;
+    // CTA ks owns tokens [t0, t1): float4 over rows, partials summed in rank order.
+    const int per = (T + splitk - 1) / splitk;
+    const int t0 = ks * per, t1 = min(T, t0 + per);
+    const int rows = a_blk ? min(spb, n_act - a0) * sh.R : BM;
+    const int n_items = (t1 - t0) * (BM / 4);
+    for (int w0 = threadIdx.x; w0 < n_items; w0 += 2 * kGemmThreads) {
+      // two work items per iteration: all their distributed-shared-memory loads are in flight at once
+      float4 pv[2][kSkinnyMaxSplit];
+      bool live[2];
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int w = w0 + h * kGemmThreads;
+        const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
+        live[h] = w < n_items && o4 < rows;
+  #pragma unroll
+        for (int r = 0; r < kSkinnyMaxSplit; ++r)
+          if (live[h] && r < splitk)
+            pv[h][r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
+      }
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!live[h]) continue;
+        const int w = w0 + h * kGemmThreads;
+        const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
+        float4 acc = pv[h][0];
+  #pragma unroll
+        for (int r = 1; r < kSkinnyMaxSplit; ++r)
+          if (r < splitk) { acc.x += pv[h][r].x; acc.y += pv[h][r].y; acc.z += pv[h][r].z; acc.w += pv[h][r].w; }
+        if (a_blk) {
+          *reinterpret_cast<float4*>(sh.vfull + static_cast<size_t>(t) * sh.vfull_ld + a0 * sh.R + o4) = acc;
+        } else {
+          const int o = o0 + o4;
+          float* dst = y + static_cast<size_t>(t) * D + o;
+          if (o + 4 <= D && (D & 3) == 0) {
+            *reinterpret_cast<float4*>(dst) = acc;
+          } else {
+            if (o < D) dst[0] = acc.x;
+            if (o + 1 < D) dst[1] = acc.y;
+            if (o + 2 < D) dst[2] = acc.z;
+            if (o + 3 < D) dst[3] = acc.w;
+          }
+        }
       }
     }
+    ptx::cluster_sync_all();                          // no CTA leaves while others read its tile
   }
-  ptx::grid_dependents_launch();                      // the expand may start its set-up
-  ptx::cluster_sync_all();                            // no CTA leaves while others read its tile
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, tmem_cols);
@@ -471,13 +511,15 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = splitk;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   note_launch_begin(kKindGemm, s);
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, T, D, K, NT, splitk, tmem_cols,
                                      err, sh);
@@ -516,7 +558,9 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
                                      const MetaView& m, uint32_t* err, int num_sms, cudaStream_t s) {
   if (m.T == 0 || pool.D == 0) return cudaSuccess;
   const int max_act = std::min(pool.S, m.n);
-  SkinnyShrink sh{m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R, (max_act * pool.R + BM - 1) / BM};
+  const int n_dchunk = (pool.D + kExpandVfullCols - 1) / kExpandVfullCols;
+  SkinnyShrink sh{pool, m, n_dchunk, m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R,
+                  (max_act * pool.R + BM - 1) / BM};
   return launch_skinny(x, W, y, m.T, pool.K, pool.D, err, num_sms, pool.A, pool.S, sh, s);
 }
 

@@ -17,6 +17,7 @@
 // With several slots per token it works per token, adding the slots in order j = 0..J-1.
 // Either way every output is a fixed sequence of fp32 operations (deterministic), tokens
 // whose slots are all -1 are never touched, and with no active pair no block does any work.
+#include "expand_vfull.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -234,116 +235,28 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
 // slot in vfull[t][a][q]. These kernels are programmatic dependents of that GEMM: everything
 // that does not depend on it (the step's metadata, the B rows, which are prefetched into L2) is
 // done before griddepcontrol.wait, and only v and y are touched after it.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // One slot per token: item = (pair-block, 512-column range), as in lora_expand_segment_kernel.
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_vfull_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
-  __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
-  __shared__ int tok[kPairBlock];
+  __shared__ ExpandSmem es;
+  ptx::grid_dependents_launch();                    // the next kernel may start its set-up
   const int items = m.counts[2] * n_dchunk;
-  const int R = pool.R, D = pool.D;
   bool waited = false;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int b = item / n_dchunk, dc = item - b * n_dchunk;
-    const int slot = m.blk_slot[b];
-    const int start = m.blk_start[b];
-    const int cnt = m.blk_count[b];
-    const int rank = pool.slot_rank[slot];
-    const float c = pool.slot_scale[slot];
-    const int rpad = (rank + 7) & ~7;
-    const int oa = dc * kExpandColsPerItem;
-    const int ob = min(D, oa + kExpandColsPerItem);
-    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads)
-      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(slot) * D + o) * R + u);
-    if (!waited) {
-      ptx::grid_dependency_wait();
-      waited = true;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
-      const int pi = i / rpad, q = i - pi * rpad;
-      const int p = m.order[start + pi];
-      vs[pi][q] = q < rank ? c * m.pair_scale[p] * m.vfull[static_cast<size_t>(p) * m.vfull_ld + m.pair_act[p] * R + q]
-                           : 0.f;
-      if (q == 0) tok[pi] = p;
-    }
-    __syncthreads();
-    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads) {
-      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
-      float d[kPairBlock];
-#pragma unroll
-      for (int i = 0; i < kPairBlock; ++i) d[i] = 0.f;
-      for (int u = 0; u < rpad / 8; ++u) {
-        const uint4 bv = __ldg(brow + u);
-#pragma unroll
-        for (int i = 0; i < kPairBlock; ++i)
-          if (i < cnt) d[i] += dot8_bf16_f32(bv, &vs[i][8 * u]);
-      }
-#pragma unroll
-      for (int i = 0; i < kPairBlock; ++i)
-        if (i < cnt) y[static_cast<size_t>(tok[i]) * D + o] += d[i];
-    }
-  }
+  for (int item = blockIdx.x; item < items; item += gridDim.x)
+    expand_vfull_segment_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
   if (!waited) ptx::grid_dependency_wait();
 }
 
 // Several slots per token: item = (token, 512-column range), slots added in order j = 0..J-1.
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_vfull_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
-  __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
-  __shared__ float cs[kMaxJ];
-  __shared__ int ss[kMaxJ], rs[kMaxJ], as[kMaxJ];
-  const int J = m.J, R = pool.R, D = pool.D;
+  __shared__ ExpandSmem es;
+  ptx::grid_dependents_launch();                    // the next kernel may start its set-up
   const int items = m.T * n_dchunk;
   bool waited = false;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int t = item / n_dchunk, dc = item - t * n_dchunk;
-    bool any = false;
-    for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0;
-    if (!any) continue;                                // uniform across the block
-    __syncthreads();
-    if (threadIdx.x < J) {
-      const int p = t * J + threadIdx.x;
-      const int s = m.pair_slot[p];
-      ss[threadIdx.x] = s;
-      rs[threadIdx.x] = s >= 0 ? pool.slot_rank[s] : 0;
-      cs[threadIdx.x] = s >= 0 ? m.pair_scale[p] * pool.slot_scale[s] : 0.f;
-      as[threadIdx.x] = m.pair_act[p];
-    }
-    __syncthreads();
-    const int oa = dc * kExpandColsPerItem;
-    const int ob = min(D, oa + kExpandColsPerItem);
-    for (int j = 0; j < J; ++j)
-      if (ss[j] >= 0)
-        for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads)
-          for (int u = 0; u < rs[j]; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(ss[j]) * D + o) * R + u);
-    if (!waited) {
-      ptx::grid_dependency_wait();
-      waited = true;
-    }
-    for (int i = threadIdx.x; i < J * R; i += kExpandThreads) {
-      const int j = i / R, q = i - j * R;
-      vs[j][q] = (ss[j] >= 0 && q < rs[j])
-                     ? cs[j] * m.vfull[static_cast<size_t>(t) * m.vfull_ld + as[j] * R + q]
-                     : 0.f;
-    }
-    __syncthreads();
-    for (int o = oa + threadIdx.x; o < ob; o += kExpandThreads) {
-      float acc = y[static_cast<size_t>(t) * D + o];
-      for (int j = 0; j < J; ++j) {
-        const int s = ss[j];
-        if (s < 0) continue;
-        const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(s) * D + o) * R);
-        float d = 0.f;
-        for (int u = 0; u < (rs[j] + 7) / 8; ++u) d += dot8_bf16_f32(__ldg(brow + u), &vs[j][8 * u]);
-        acc += d;
-      }
-      y[static_cast<size_t>(t) * D + o] = acc;
-    }
-  }
+  for (int item = blockIdx.x; item < items; item += gridDim.x)
+    expand_vfull_token_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
   if (!waited) ptx::grid_dependency_wait();
 }
 
@@ -399,7 +312,7 @@ cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m
 cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
                                      cudaStream_t s) {
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
-  const int n_dchunk = (pool.D + kExpandColsPerItem - 1) / kExpandColsPerItem;
+  const int n_dchunk = (pool.D + kExpandVfullCols - 1) / kExpandVfullCols;
   const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
   int grid = num_sms * 8;
   if (grid > max_items) grid = max_items;

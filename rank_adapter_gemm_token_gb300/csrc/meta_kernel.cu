@@ -65,6 +65,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __shared__ int first_bad;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  ptx::grid_dependents_launch();             // the first linear's GEMM may start its set-up
   // 0. which slots hold an adapter (staged once, so pair validation needs no dependent load);
   //    `cursor` is free until step 2
   for (int b = tid; b < nb; b += kMetaThreads) {

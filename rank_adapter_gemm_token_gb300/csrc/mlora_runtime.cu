@@ -140,7 +140,13 @@ struct mlora_pool {
   cudaStream_t copy_stream = nullptr;
   bool own_stream = false;
   cudaEvent_t load_done = nullptr, use_done = nullptr;
-  bool has_load = false, has_use = false;
+  bool has_load = false;
+  uint64_t load_seq = 0;                       // number of loads/clears queued so far
+  // Streams that have read this pool, with the load_seq each last waited for. A load orders
+  // itself after all work already queued on them (write-after-read); a compute call waits for
+  // the loads only when one was queued since its stream last waited. No event is recorded on
+  // the compute path.
+  std::vector<std::pair<cudaStream_t, uint64_t>> users;
   std::mutex mu;
 
   PoolView view() const { return PoolView{A, B, slot_scale, slot_rank, S, R, K, D}; }
@@ -160,6 +166,7 @@ struct mlora_meta {
   int T = 0, J = 1, S = -1;
   bool built = false;
   cudaEvent_t done = nullptr;
+  cudaStream_t last_stream = nullptr;          // the stream of the last call that used the metadata
 
   MetaView view() const {
     return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count, counts,
@@ -266,7 +273,7 @@ mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_
 mlora_status mlora_pool_destroy(mlora_pool_t p) {
   if (!p) return MLORA_OK;
   if (p->has_load) cudaEventSynchronize(p->load_done);
-  if (p->has_use) cudaEventSynchronize(p->use_done);
+  for (auto& u : p->users) cudaStreamSynchronize(u.first);
   if (p->copy_stream) cudaStreamSynchronize(p->copy_stream);
   if (p->own_stream && p->copy_stream) cudaStreamDestroy(p->copy_stream);
   if (p->load_done) cudaEventDestroy(p->load_done);
@@ -282,7 +289,10 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
 static mlora_status write_slot(mlora_pool_t p, int slot, const mlora_bf16* A_host, const mlora_bf16* B_host,
                                int rank, float alpha, int rslora) {
   cudaStream_t cs = p->copy_stream;
-  if (p->has_use) MLORA_CUDA(cudaStreamWaitEvent(cs, p->use_done, 0), "wait for last use of the pool");
+  for (auto& u : p->users) {                   // after every call already queued on the pool
+    MLORA_CUDA(cudaEventRecord(p->use_done, u.first), "record use event");
+    MLORA_CUDA(cudaStreamWaitEvent(cs, p->use_done, 0), "wait for last use of the pool");
+  }
   uint16_t* a_slot = p->A + static_cast<size_t>(slot) * p->R * p->K;
   uint16_t* b_slot = p->B + static_cast<size_t>(slot) * p->D * p->R;
   MLORA_CUDA(cudaMemsetAsync(a_slot, 0, static_cast<size_t>(p->R) * p->K * 2, cs), "zero slot A");
@@ -301,6 +311,7 @@ static mlora_status write_slot(mlora_pool_t p, int slot, const mlora_bf16* A_hos
   if (e != cudaSuccess) return cuda_fail(e, "set_slot_kernel");
   MLORA_CUDA(cudaEventRecord(p->load_done, cs), "record load event");
   p->has_load = true;
+  ++p->load_seq;
   p->h_rank[slot] = rank;
   return MLORA_OK;
 }
@@ -345,6 +356,24 @@ mlora_status mlora_pool_info(mlora_pool_t p, int* n_slots, int* r_pad, int* K, i
   if (B_pool) *B_pool = p->B;
   if (slot_scale) *slot_scale = p->slot_scale;
   if (slot_rank) *slot_rank = p->slot_rank;
+  return MLORA_OK;
+}
+
+// Orders stream s after the pool's queued loads (only if one was queued since s last waited)
+// and remembers s as a user of the pool.
+static mlora_status pool_use(mlora_pool_t p, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(p->mu);
+  for (auto& u : p->users) {
+    if (u.first == s) {
+      if (p->has_load && u.second != p->load_seq) {
+        MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
+        u.second = p->load_seq;
+      }
+      return MLORA_OK;
+    }
+  }
+  if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
+  p->users.emplace_back(s, p->load_seq);
   return MLORA_OK;
 }
 
@@ -439,21 +468,28 @@ mlora_status mlora_build_meta(mlora_meta_t m, const int32_t* token_slots, const 
   if (pool->R > m->R_max)
     return fail(MLORA_ERR_MISMATCH, "pool rank width %d exceeds the metadata's %d", pool->R, m->R_max);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pool->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, pool->load_done, 0), "wait for slot loads");
+  if (mlora_status st = pool_use(pool, s)) return st;
   m->T = T;
   m->J = J;
   m->S = pool->S;
   MetaView v = m->view();
   cudaError_t e = launch_build_meta(token_slots, scales, T, J, pool->S, pool->slot_rank, v, s);
   if (e != cudaSuccess) return cuda_fail(e, "build_meta launch");
-  MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
+  m->last_stream = s;
   m->built = true;
+  return MLORA_OK;
+}
+
+// Waits for every call queued so far on the metadata's last stream.
+static mlora_status meta_sync(mlora_meta_t m) {
+  MLORA_CUDA(cudaEventRecord(m->done, m->last_stream), "record meta event");
+  MLORA_CUDA(cudaEventSynchronize(m->done), "meta sync");
   return MLORA_OK;
 }
 
 mlora_status mlora_meta_status(mlora_meta_t m) {
   if (!m) return fail(MLORA_ERR_INVALID_ARG, "meta is NULL");
-  MLORA_CUDA(cudaEventSynchronize(m->done), "meta sync");
+  if (mlora_status st = meta_sync(m)) return st;
   uint32_t err = 0, gerr = 0;
   int32_t counts[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   MLORA_CUDA(cudaMemcpy(&err, m->err, 4, cudaMemcpyDeviceToHost), "read meta error word");
@@ -478,7 +514,7 @@ mlora_status mlora_meta_read(mlora_meta_t m, int32_t* order, int32_t* seg_slot, 
                              int* n_active) {
   if (!m) return fail(MLORA_ERR_INVALID_ARG, "meta is NULL");
   if (!m->built) return fail(MLORA_ERR_INVALID_ARG, "metadata has not been built");
-  MLORA_CUDA(cudaEventSynchronize(m->done), "meta sync");
+  if (mlora_status st = meta_sync(m)) return st;
   int32_t counts[8];
   MLORA_CUDA(cudaMemcpy(counts, m->counts, 32, cudaMemcpyDeviceToHost), "read counts");
   const size_t n = static_cast<size_t>(m->T) * m->J;
@@ -530,11 +566,10 @@ mlora_status mlora_lora_shrink(mlora_pool_t p, mlora_meta_t m, const mlora_bf16*
   DeviceState* ds = nullptr;
   if (mlora_status st = device_state(&ds)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
+  if (mlora_status st = pool_use(p, s)) return st;
   cudaError_t e = launch_lora_shrink(x, p->view(), m->view(), ds->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
-  MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
-  p->has_use = true;
+  m->last_stream = s;
   return MLORA_OK;
 }
 
@@ -544,12 +579,10 @@ mlora_status mlora_lora_expand(mlora_pool_t p, mlora_meta_t m, float* y, void* s
   DeviceState* ds = nullptr;
   if (mlora_status st = device_state(&ds)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
+  if (mlora_status st = pool_use(p, s)) return st;
   cudaError_t e = launch_lora_expand(y, p->view(), m->view(), ds->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "expand launch");
-  MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
-  MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
-  p->has_use = true;
+  m->last_stream = s;
   return MLORA_OK;
 }
 
@@ -560,7 +593,7 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   DeviceState* ds = nullptr;
   if (mlora_status st = device_state(&ds)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p->has_load) MLORA_CUDA(cudaStreamWaitEvent(s, p->load_done, 0), "wait for slot loads");
+  if (mlora_status st = pool_use(p, s)) return st;
   const MetaView mv = m->view();
   const PoolView pv = p->view();
   cudaError_t e = cudaSuccess;
@@ -576,9 +609,7 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
     if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "shrink launch");
     if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
   }
-  MLORA_CUDA(cudaEventRecord(p->use_done, s), "record use event");
-  MLORA_CUDA(cudaEventRecord(m->done, s), "record meta event");
-  p->has_use = true;
+  m->last_stream = s;
   return MLORA_OK;
 }
 
