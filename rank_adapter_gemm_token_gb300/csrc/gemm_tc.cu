@@ -42,10 +42,21 @@ struct GemmSmem {
   static constexpr int kBytes = kBarrierOffset + 256 + 1024;   // + barriers, + alignment slack
 };
 
+// Extra K blocks of the fused side path: for an M-tile whose tokens use at most kTileSlots slots,
+// one 64-wide block per slot with A operand = the scaled v tile (tensor-core shrink output) and
+// B operand = the slot's B rows of the N tile, both fetched by TMA into the same stage layout.
+__device__ __forceinline__ int extra_kblocks(const int32_t* tile_info, int m_blk) {
+  if (!tile_info) return 0;
+  const int c = tile_info[m_blk * (kTileSlots + 1)];
+  return c <= kTileSlots ? c : 0;
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                    float* __restrict__ y, int T, int D, int K, uint32_t* __restrict__ err) {
+                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_b,
+                    const int32_t* __restrict__ tile_info, float* __restrict__ y, int T, int D, int K,
+                    uint32_t* __restrict__ err) {
   using L = GemmSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -91,15 +102,24 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * BM;
+        const int m_blk = tile % num_m;
+        const int m0 = m_blk * BM;
         const int n0 = (tile / num_m) * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int n_extra = extra_kblocks(tile_info, m_blk);
+        for (int kb = 0; kb < num_kb + n_extra; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) { ok = false; break; }
           uint8_t* sa = smem + stage * L::kStageBytes;
           uint8_t* sb = sa + L::kABytes;
           ptx::mbar_arrive_expect_tx(&full[stage], L::kStageBytes);
-          ptx::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, m0);
-          ptx::tma_load_2d(sb, &tmap_w, &full[stage], kb * BK, n0);
+          if (kb < num_kb) {
+            ptx::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, m0);
+            ptx::tma_load_2d(sb, &tmap_w, &full[stage], kb * BK, n0);
+          } else {
+            const int i = kb - num_kb;
+            const int slot = tile_info[m_blk * (kTileSlots + 1) + 1 + i];
+            ptx::tma_load_2d(sa, &tmap_v, &full[stage], 0, (m_blk * kTileSlots + i) * BM);
+            ptx::tma_load_2d(sb, &tmap_b, &full[stage], 0, slot * D + n0);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -117,7 +137,8 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
         if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, err)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int n_kb = num_kb + extra_kblocks(tile_info, tile % num_m);
+        for (int kb = 0; kb < n_kb; ++kb) {
           if (!ptx::mbar_wait(&full[stage], phase, err)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(smem + stage * L::kStageBytes);
@@ -435,7 +456,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // Row-major bf16 matrix [rows, cols] seen as a 2-D tensor, box = box_cols x box_rows, 128B swizzle.
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, int box_cols) {
+bool make_tmap_bf16_impl(CUtensorMap* map, const void* base, long rows, int cols, int box_rows, int box_cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -450,7 +471,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rows, int cols, int 
 
 template <int BN, int STAGES>
 cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
-                      int num_sms, cudaStream_t s) {
+                      int num_sms, const PoolView* pool, const MetaView* meta, cudaStream_t s) {
   using L = GemmSmem<BN, STAGES>;
   static int configured_device = -1;
   int dev = 0;
@@ -461,13 +482,24 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap mx, mw;
-  if (!make_tmap_bf16(&mx, x, T, K, BM, BK) || !make_tmap_bf16(&mw, W, D, K, BN, BK))
+  CUtensorMap mx, mw, mv, mb;
+  if (!make_tmap_bf16_impl(&mx, x, T, K, BM, BK) || !make_tmap_bf16_impl(&mw, W, D, K, BN, BK))
     return cudaErrorInvalidValue;
+  const int32_t* tile_info = nullptr;
+  if (pool && meta) {                     // the fused side path: v tiles and the pool's B rows
+    const long v_rows = static_cast<long>((T + BM - 1) / BM) * kTileSlots * BM;
+    if (!make_tmap_bf16_impl(&mv, meta->vtile, v_rows, BK, BM, BK) ||
+        !make_tmap_bf16_impl(&mb, pool->B, static_cast<long>(pool->S) * D, pool->R, BN, BK))
+      return cudaErrorInvalidValue;
+    tile_info = meta->tile_info;
+  } else {
+    mv = mx;
+    mb = mw;
+  }
   const int tiles = ((T + BM - 1) / BM) * ((D + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   note_launch_begin(kKindGemm, s);
-  gemm_bf16_tc_kernel<BN, STAGES><<<grid, kGemmThreads, L::kBytes, s>>>(mx, mw, y, T, D, K, err);
+  gemm_bf16_tc_kernel<BN, STAGES><<<grid, kGemmThreads, L::kBytes, s>>>(mx, mw, mv, mb, tile_info, y, T, D, K, err);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindGemm, s);
   return e;
@@ -500,9 +532,9 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
     configured_device = dev;
   }
   CUtensorMap mw, mx, ma;
-  if (!make_tmap_bf16(&mw, W, D, K, BM, BK) || !make_tmap_bf16(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
   if (sh.n_ablk > 0) {
-    if (!make_tmap_bf16(&ma, A_pool, S * sh.R, K, sh.R, BK)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_impl(&ma, A_pool, static_cast<long>(S) * sh.R, K, sh.R, BK)) return cudaErrorInvalidValue;
   } else {
     ma = mw;
   }
@@ -529,18 +561,30 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
 
 }  // namespace
 
-cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
-                             uint32_t* err, int num_sms, cudaStream_t s) {
+bool make_tmap_bf16(CUtensorMap* map, const void* base, long rows, int cols, int box_rows, int box_cols) {
+  return make_tmap_bf16_impl(map, base, rows, cols, box_rows, box_cols);
+}
+
+cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
+                                  uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
+                                  cudaStream_t s) {
   if (T == 0 || D == 0) return cudaSuccess;
-  if (T <= kSkinnyMaxT) {
+  if (T <= kSkinnyMaxT && !pool) {
     SkinnyShrink none{};
     return launch_skinny(x, W, y, T, K, D, err, num_sms, nullptr, 0, none, s);
   }
   // Largest N tile that still gives every SM a tile; small problems take N = 64.
   const int m_tiles = (T + BM - 1) / BM;
-  if (m_tiles * ((D + 255) / 256) >= num_sms) return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, s);
-  if (m_tiles * ((D + 127) / 128) >= num_sms) return launch_tc<128, 6>(x, W, y, T, K, D, err, num_sms, s);
-  return launch_tc<64, 8>(x, W, y, T, K, D, err, num_sms, s);
+  if (m_tiles * ((D + 255) / 256) >= num_sms)
+    return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
+  if (m_tiles * ((D + 127) / 128) >= num_sms)
+    return launch_tc<128, 6>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
+  return launch_tc<64, 8>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
+}
+
+cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
+                             uint32_t* err, int num_sms, cudaStream_t s) {
+  return launch_base_gemm_lora(x, W, y, T, K, D, err, num_sms, nullptr, nullptr, s);
 }
 
 }  // namespace mlora

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mlora {
@@ -13,6 +14,8 @@ constexpr int kMaxJ = 8;            // adapter slots per token
 constexpr int kPairBlock = 16;      // pairs of one slot handled together by the shrink
 constexpr int kMetaThreads = 1024;
 constexpr int kMaxShrinkSplits = 16;   // K splits of the shrink (partial sums per split)
+constexpr int kMaxTiles = 512;         // 128-token M-tiles of a step (65535 tokens)
+constexpr int kTileSlots = 4;          // slots per M-tile handled on the tensor cores
 
 // Device arrays of one adapter pool (one adapted linear).
 struct PoolView {
@@ -41,6 +44,10 @@ struct MetaView {
   float* vpart;         // shrink output: [n_splits][n][R] fp32 partial sums of A x per K split
   float* vfull;         // small-batch shrink output: [T][act][R] fp32, row stride vfull_ld floats
   int vfull_ld;
+  int32_t* tile_info;   // per 128-token M-tile: [count, slot_0 .. slot_{kTileSlots-1}] (ascending,
+                        //   -1 unused); count > kTileSlots = too many slots (overflow tile)
+  int32_t* pair_fused;  // [n] 1: the pair's side path runs on the tensor cores inside the GEMM
+  uint16_t* vtile;      // tensor-core shrink output: [tiles][kTileSlots][128][64] bf16, s c v per token
   int n;                // pairs of the current step (T * J)
   int T, J;
 };
@@ -60,6 +67,10 @@ int report_cuda_error(cudaError_t e, const char* what);
 // Launch counter + tracing hooks (mlora_runtime.cu).
 void note_launch_begin(int kind, cudaStream_t s);
 void note_launch_end(int kind, cudaStream_t s);
+
+// Row-major bf16 matrix [rows, cols] as a TMA tensor map with a box of box_rows x box_cols and
+// the 128-byte swizzle (gemm_tc.cu). False if the encoder is unavailable or rejects it.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, long rows, int cols, int box_rows, int box_cols);
 
 // Launchers. Each returns the cudaError_t of its launch.
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
@@ -81,10 +92,23 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
 cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
                                      cudaStream_t s);
 
+// Tensor-core prefill path (sgmv_tc.cu): pools with padded rank R == 64.
+bool sgmv_tc_supported(int R);
+// vtile = scaled (x A_slot^T) per (M-tile, slot) for tiles with at most kTileSlots slots.
+cudaError_t launch_sgmv_shrink_tc(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
+                                  cudaStream_t s);
+// Tiled base GEMM; with pool and meta it also adds vtile x B_slot^T as extra K blocks of the
+// fused tiles.
+cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
+                                  uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
+                                  cudaStream_t s);
+
 // K elements per shrink split and the number of splits for a pool of width R.
 void shrink_split(int K, int R, int* kc_len, int* n_ks);
+// CUDA-core shrink / expand; with skip_fused they leave out the pairs the tensor-core path handles.
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s);
-cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s);
+                               cudaStream_t s, bool skip_fused = false);
+cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
+                               bool skip_fused = false);
 
 }  // namespace mlora

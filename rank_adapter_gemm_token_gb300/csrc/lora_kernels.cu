@@ -60,7 +60,7 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4& b, const float* v) {
 // every SM, and the kernel lets a dependent kernel (programmatic launch) start right away.
 template <int RPW>
 __global__ void __launch_bounds__(kShrinkThreads)
-lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, int kc_len, int n_ks) {
+lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, int kc_len, int n_ks, int skip_fused) {
   constexpr int G = 4;                                        // pairs per register group
   constexpr int V = 8 / RPW;                                  // vectors per lane per row
   ptx::grid_dependents_launch();
@@ -73,6 +73,11 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
+    if (skip_fused) {                                         // all pairs done on the tensor cores?
+      bool todo = false;
+      for (int i = 0; i < cnt; ++i) todo |= !m.pair_fused[m.order[start + i]];
+      if (!todo) continue;                                    // uniform across the block
+    }
     const int k0 = ks * kc_len;
     const int nv = (min(K, k0 + kc_len) - k0) / 8;            // vectors in this split
     for (int qg = warp; qg < rank; qg += 8 * RPW) {           // rows qg + 8 i, i < RPW
@@ -146,7 +151,8 @@ __device__ __forceinline__ float pair_v(const MetaView& m, int R, int n_ks, int 
 // updates y[t][o] for every token of the block (consecutive o, coalesced). Each y element is
 // updated by exactly one pair, so the result is deterministic.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk) {
+lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk,
+                           int skip_fused) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
   const int items = m.counts[2] * n_dchunk;
@@ -159,12 +165,18 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
     const int rank = pool.slot_rank[slot];
     const float c = pool.slot_scale[slot];
     const int rpad = (rank + 7) & ~7;
+    if (skip_fused) {                                         // all pairs done on the tensor cores?
+      bool todo = false;
+      for (int i = 0; i < cnt; ++i) todo |= !m.pair_fused[m.order[start + i]];
+      if (!todo) continue;                                    // uniform across the block
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
       const int pi = i / rpad, q = i - pi * rpad;
       const int p = m.order[start + pi];
-      vs[pi][q] = pair_v(m, R, n_ks, p, q, rank, c * m.pair_scale[p]);
-      if (q == 0) tok[pi] = p;                      // J == 1: token index == pair index
+      const bool done = skip_fused && m.pair_fused[p];        // added inside the base GEMM
+      vs[pi][q] = done ? 0.f : pair_v(m, R, n_ks, p, q, rank, c * m.pair_scale[p]);
+      if (q == 0) tok[pi] = done ? -1 : p;          // J == 1: token index == pair index
     }
     __syncthreads();
     for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
@@ -181,7 +193,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
       }
 #pragma unroll
       for (int i = 0; i < kPairBlock; ++i)
-        if (i < cnt) y[static_cast<size_t>(tok[i]) * D + o] += d[i];
+        if (i < cnt && tok[i] >= 0) y[static_cast<size_t>(tok[i]) * D + o] += d[i];
     }
   }
 }
@@ -189,7 +201,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
 // J > 1: item = (token, 512-column range); slots are added in order j = 0..J-1 so every output
 // is a fixed sequence of fp32 additions. Thread c owns column o: B rows and y coalesced.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk) {
+lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk, int skip_fused) {
   __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
@@ -198,12 +210,12 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int t = item / n_dchunk, dc = item - t * n_dchunk;
     bool any = false;
-    for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0;
+    for (int j = 0; j < J; ++j) any |= m.pair_slot[t * J + j] >= 0 && !(skip_fused && m.pair_fused[t * J + j]);
     if (!any) continue;                                // uniform across the block
     __syncthreads();
     if (threadIdx.x < J) {
       const int p = t * J + threadIdx.x;
-      const int s = m.pair_slot[p];
+      const int s = (skip_fused && m.pair_fused[p]) ? -1 : m.pair_slot[p];
       ss[threadIdx.x] = s;
       rs[threadIdx.x] = s >= 0 ? pool.slot_rank[s] : 0;
       cs[threadIdx.x] = s >= 0 ? m.pair_scale[p] * pool.slot_scale[s] : 0.f;
@@ -272,7 +284,7 @@ void shrink_split(int K, int R, int* kc_len, int* n_ks) {
 }
 
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool skip_fused) {
   if (m.n == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
@@ -281,17 +293,18 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindShrink, s);
   switch (shrink_rows_per_warp(pool.R)) {
-    case 1: lora_shrink_kernel<1><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
-    case 2: lora_shrink_kernel<2><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
-    case 4: lora_shrink_kernel<4><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
-    default: lora_shrink_kernel<8><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks); break;
+    case 1: lora_shrink_kernel<1><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
+    case 2: lora_shrink_kernel<2><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
+    case 4: lora_shrink_kernel<4><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
+    default: lora_shrink_kernel<8><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
   }
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindShrink, s);
   return e;
 }
 
-cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s) {
+cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
+                               bool skip_fused) {
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
@@ -301,9 +314,9 @@ cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindExpand, s);
   if (m.J == 1)
-    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk);
+    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip_fused);
   else
-    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk);
+    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip_fused);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindExpand, s);
   return e;

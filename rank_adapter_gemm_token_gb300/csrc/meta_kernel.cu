@@ -63,6 +63,8 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
+  __shared__ int tile_cnt[kMaxTiles];                    // distinct slots per 128-token M-tile
+  __shared__ int tile_list[kMaxTiles * kTileSlots];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   ptx::grid_dependents_launch();             // the first linear's GEMM may start its set-up
@@ -165,6 +167,45 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     for (int b = tid; b < nb; b += kMetaThreads) cursor[b] += chunk_tot[b];
     __syncthreads();
   }
+
+  // 4. slots of each 128-token M-tile (x order), for the tensor-core prefill path: within a
+  //    segment the pairs are in token order, so the first pair of each (slot, tile) run adds the
+  //    slot to that tile's list; a tile with more than kTileSlots slots overflows.
+  const int n_tiles = (m.T + 127) / 128;
+  for (int i = tid; i < n_tiles; i += kMetaThreads) tile_cnt[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kMetaThreads) {
+    const int p = m.order[i];
+    const int s = m.pair_slot[p];
+    if (s < 0) continue;
+    const int tile = (p / m.J) >> 7;
+    bool first = true;
+    if (i > 0) {
+      const int q = m.order[i - 1];
+      first = m.pair_slot[q] != s || ((q / m.J) >> 7) != tile;
+    }
+    if (first) {
+      const int k = atomicAdd(&tile_cnt[tile], 1);
+      if (k < kTileSlots) tile_list[tile * kTileSlots + k] = s;
+    }
+  }
+  __syncthreads();
+  for (int tile = tid; tile < n_tiles; tile += kMetaThreads) {   // ascending slot order per tile
+    const int c = tile_cnt[tile];
+    int* l = &tile_list[tile * kTileSlots];
+    const int k = c < kTileSlots ? c : kTileSlots;
+    for (int a = 1; a < k; ++a)
+      for (int b = a; b > 0 && l[b - 1] > l[b]; --b) {
+        const int t = l[b];
+        l[b] = l[b - 1];
+        l[b - 1] = t;
+      }
+    m.tile_info[tile * (kTileSlots + 1)] = c;
+    for (int a = 0; a < kTileSlots; ++a) m.tile_info[tile * (kTileSlots + 1) + 1 + a] = a < k ? l[a] : -1;
+  }
+  __syncthreads();
+  for (int p = tid; p < n; p += kMetaThreads)
+    m.pair_fused[p] = m.pair_slot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
 
   if (tid == 0) {
     m.counts[3] = first_bad;

@@ -163,6 +163,8 @@ struct mlora_meta {
   float* vpart = nullptr;
   float* vfull = nullptr;
   int vfull_ld = 0;
+  int32_t *tile_info = nullptr, *pair_fused = nullptr;
+  uint16_t* vtile = nullptr;
   int T = 0, J = 1, S = -1;
   bool built = false;
   cudaEvent_t done = nullptr;
@@ -170,7 +172,8 @@ struct mlora_meta {
 
   MetaView view() const {
     return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count, counts,
-                    pair_act, act_slot, err, vpart, vfull, vfull_ld, T * J, T, J};
+                    pair_act, act_slot, err, vpart, vfull, vfull_ld, tile_info, pair_fused, vtile,
+                    T * J, T, J};
   }
 };
 
@@ -415,6 +418,11 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->act_slot), (n + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->err), 4);
   alloc(reinterpret_cast<void**>(&m->vpart), static_cast<size_t>(kMaxShrinkSplits) * n * m->R_max * 4);
+  // tensor-core prefill path: per-tile slot lists, fused-pair flags, scaled v tiles (bf16)
+  const size_t n_tiles = (static_cast<size_t>(max_tokens) + 127) / 128;
+  alloc(reinterpret_cast<void**>(&m->tile_info), n_tiles * (kTileSlots + 1) * 4);
+  alloc(reinterpret_cast<void**>(&m->pair_fused), n * 4);
+  alloc(reinterpret_cast<void**>(&m->vtile), n_tiles * kTileSlots * 128 * 64 * 2);
   // small-batch shrink output: v of every token (up to 256) against every active slot
   const int vt = std::min(max_tokens, kVfullMaxTokens);
   m->vfull_ld = std::min(m->n_max, kVfullMaxAct) * m->R_max;
@@ -453,6 +461,9 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->vfull);
   cudaFree(m->pair_act);
   cudaFree(m->act_slot);
+  cudaFree(m->tile_info);
+  cudaFree(m->pair_fused);
+  cudaFree(m->vtile);
   delete m;
   return MLORA_OK;
 }
@@ -603,6 +614,14 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
     if ((e = launch_gemm_shrink_fused(x, W, y, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "fused GEMM launch");
     if ((e = launch_lora_expand_vfull(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
+  } else if (m->T > kSkinnyMaxT && sgmv_tc_supported(p->R)) {
+    // larger batch, rank width 64: tiles whose tokens use few slots get the shrink on the tensor
+    // cores and the expand as extra K blocks of the base GEMM; the rest take the CUDA-core path
+    if ((e = launch_sgmv_shrink_tc(x, pv, mv, ds->err, s)) != cudaSuccess) return cuda_fail(e, "SGMV shrink launch");
+    if ((e = launch_base_gemm_lora(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, &pv, &mv, s)) != cudaSuccess)
+      return cuda_fail(e, "base GEMM launch");
+    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "shrink launch");
+    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "expand launch");
   } else {
     if ((e = launch_base_gemm(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");

@@ -222,3 +222,35 @@ def test_clear_slot_makes_it_empty(cuda_device):
             dw.meta.status()
         assert e.value.status == mlora.MLORA_ERR_BAD_TOKEN_SLOT
     dw.close()
+
+
+@pytest.mark.parametrize("J,seed", [(1, 5), (2, 6)])
+def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed):
+    """T > 256 with r_max 64: runs of one slot (M-tiles with at most 4 slots: shrink on the tensor
+    cores, expand inside the base GEMM) followed by per-token random slots (tiles with more
+    slots: CUDA-core path). Ragged T, K and D; mixed ranks; a second slot per token for J = 2."""
+    rng = np.random.default_rng(seed)
+    T, K, D, S, R = 700, 320, 392, 12, 64
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = (8, 16, 64, 40)[s % 4]
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(seed, 300 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(2 * r), rslora=bool(s % 3 == 0))
+    slots = np.full((T, J), -1, dtype=np.int32)
+    t = 0
+    while t < 500:                                  # segments of one slot (some of them -1)
+        n = int(rng.integers(40, 170))
+        slots[t:t + n, 0] = int(rng.integers(-1, S))
+        t += n
+    slots[500:, 0] = rng.integers(-1, S, size=T - 500)
+    if J == 2:
+        slots[:, 1] = np.where(rng.uniform(size=T) < 0.5, rng.integers(0, S, size=T), -1)
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("tc-prefill", seed, T, J, S, R, slots, scales,
+                        {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
+    dw.close()
