@@ -88,6 +88,7 @@ __device__ __forceinline__ void expand_vfull_segment_item(float* __restrict__ y,
   __syncthreads();
   if (!*waited) {
     ptx::grid_dependency_wait();                   // v and y of the fused GEMM are complete
+    ptx::grid_dependents_launch();                 // dependents start only after this wait
     *waited = true;
   }
   for (int i = threadIdx.x; i < cnt * rpad; i += NT) {
@@ -98,21 +99,23 @@ __device__ __forceinline__ void expand_vfull_segment_item(float* __restrict__ y,
   __syncthreads();
   for (int o = oa + threadIdx.x; o < ob; o += NT) {
     const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
-    float yv[kPairBlock];
+    for (int g = 0; g < cnt; g += 4) {               // pairs in groups of four (few registers)
+      float yv[4], d[4];
 #pragma unroll
-    for (int i = 0; i < kPairBlock; ++i) yv[i] = i < cnt ? y[static_cast<size_t>(es.tok[i]) * D + o] : 0.f;
-    float d[kPairBlock];
+      for (int i = 0; i < 4; ++i) {
+        yv[i] = g + i < cnt ? y[static_cast<size_t>(es.tok[g + i]) * D + o] : 0.f;
+        d[i] = 0.f;
+      }
+      for (int u = 0; u < rpad / 8; ++u) {
+        const uint4 bv = __ldg(brow + u);
 #pragma unroll
-    for (int i = 0; i < kPairBlock; ++i) d[i] = 0.f;
-    for (int u = 0; u < rpad / 8; ++u) {
-      const uint4 bv = __ldg(brow + u);
+        for (int i = 0; i < 4; ++i)
+          if (g + i < cnt) d[i] += ev_dot8(bv, &es.vs[g + i][8 * u]);
+      }
 #pragma unroll
-      for (int i = 0; i < kPairBlock; ++i)
-        if (i < cnt) d[i] += ev_dot8(bv, &es.vs[i][8 * u]);
+      for (int i = 0; i < 4; ++i)
+        if (g + i < cnt) y[static_cast<size_t>(es.tok[g + i]) * D + o] = yv[i] + d[i];
     }
-#pragma unroll
-    for (int i = 0; i < kPairBlock; ++i)
-      if (i < cnt) y[static_cast<size_t>(es.tok[i]) * D + o] = yv[i] + d[i];
   }
 }
 
@@ -143,6 +146,7 @@ __device__ __forceinline__ void expand_vfull_token_item(float* __restrict__ y, c
         for (int o = oa + threadIdx.x; o < ob; o += NT)
           for (int u = 0; u < es.rs[j]; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(es.ss[j]) * D + o) * R + u);
     ptx::grid_dependency_wait();
+    ptx::grid_dependents_launch();
     *waited = true;
   }
   for (int i = threadIdx.x; i < J * R; i += NT) {

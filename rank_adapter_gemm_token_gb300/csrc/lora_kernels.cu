@@ -252,24 +252,28 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_vfull_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
   __shared__ ExpandSmem es;
-  ptx::grid_dependents_launch();                    // the next kernel may start its set-up
   const int items = m.counts[2] * n_dchunk;
   bool waited = false;
   for (int item = blockIdx.x; item < items; item += gridDim.x)
     expand_vfull_segment_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
-  if (!waited) ptx::grid_dependency_wait();
+  if (!waited) {
+    ptx::grid_dependency_wait();
+    ptx::grid_dependents_launch();
+  }
 }
 
 // Several slots per token: item = (token, 512-column range), slots added in order j = 0..J-1.
 __global__ void __launch_bounds__(kExpandThreads)
 lora_expand_vfull_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
   __shared__ ExpandSmem es;
-  ptx::grid_dependents_launch();                    // the next kernel may start its set-up
   const int items = m.T * n_dchunk;
   bool waited = false;
   for (int item = blockIdx.x; item < items; item += gridDim.x)
     expand_vfull_token_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
-  if (!waited) ptx::grid_dependency_wait();
+  if (!waited) {
+    ptx::grid_dependency_wait();
+    ptx::grid_dependents_launch();
+  }
 }
 
 }  // namespace
