@@ -304,6 +304,13 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   if (a_blk) {
     n_act = *sh.n_act;
     idle = a0 >= n_act;                                 // uniform across the cluster
+    if (!idle && warp == 2) {                           // this block's adapter rows into L2
+      const int n_box = min(spb, n_act - a0);
+      for (int e = lane; e < n_box * (kb1 - kb0); e += 32) {
+        const int i = e % n_box, kb = kb0 + e / n_box;
+        ptx::tma_prefetch_l2_2d(&tmap_a, kb * BK, sh.act_slot[a0 + i] * sh.R);
+      }
+    }
   }
   const int n_exp_items = sh.n_dchunk ? (sh.meta.J == 1 ? sh.meta.counts[2] : sh.meta.T) * sh.n_dchunk : 0;
 
