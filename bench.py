@@ -101,16 +101,33 @@ def algorithmic_bytes(wl) -> dict:
     (R rows each, the pool's padded rank) + v write (T x active slots x R, fp32); expand = B rows
     of the active slots at the true rank padded to 8 + read and write of y rows with an active
     slot + v reads of the active pairs.
-    Larger batches: base_gemm = W + x + y; shrink = A rows at the true rank + x rows of active
-    tokens + v partial writes; expand = B rows + y read-modify-write + v reads.
+    Larger batches with rank width 64, 128-token tiles of at most four slots (tensor-core path):
+    shrink = A rows (64 per slot) + x rows of those tiles + the scaled bf16 v tiles written;
+    base_gemm = W + x + y + those v tiles read again + B rows (64 columns per slot). Pairs in
+    tiles with more slots, and every pair of other larger batches: shrink = A rows at the true
+    rank + x rows of active tokens + v partial writes; expand = B rows + y read-modify-write +
+    v reads.
     Flops: 2*T*K*D per linear for the base product."""
     slots = wl.token_slots
     active = slots >= 0
-    act_rows = int(np.any(active, axis=1).sum())
-    pairs = int(active.sum())
-    distinct = sorted(set(int(s) for s in slots[active]))
     R = (wl.r_max + 7) // 8 * 8
     small = wl.T <= 256
+    tensor_core = not small and R == 64
+    fused = np.zeros_like(active)
+    tile_slots = []                                   # distinct slots of each fused 128-token tile
+    if tensor_core:
+        for t0 in range(0, wl.T, 128):
+            d = set(int(s) for s in slots[t0:t0 + 128][active[t0:t0 + 128]])
+            if len(d) <= 4:
+                fused[t0:t0 + 128] = active[t0:t0 + 128]
+                tile_slots.append((min(128, wl.T - t0), d))
+    rest = active & ~fused
+    act_rows = int(np.any(rest, axis=1).sum())
+    pairs = int(rest.sum())
+    distinct = sorted(set(int(s) for s in slots[rest]))
+    tc_slots = sorted(set().union(*(d for _, d in tile_slots))) if tile_slots else []
+    tc_rows = sum(rows for rows, d in tile_slots if d)
+    tc_vtile = sum(rows * len(d) * 64 * 2 for rows, d in tile_slots)
     out = {"base_gemm": 0, "shrink": 0, "expand": 0, "base_flops": 0, "meta": wl.T * wl.J * 4 * 6}
     for l in wl.linears:
         out["base_gemm"] += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
@@ -120,7 +137,11 @@ def algorithmic_bytes(wl) -> dict:
         if small:
             out["base_gemm"] += len(distinct) * R * l.K * 2 + wl.T * len(distinct) * R * 4
             out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
-        else:
+            continue
+        if tc_slots:
+            out["shrink"] += len(tc_slots) * 64 * l.K * 2 + tc_rows * l.K * 2 + tc_vtile
+            out["base_gemm"] += tc_vtile + len(tc_slots) * 64 * l.D * 2
+        if pairs:
             out["shrink"] += ra * l.K * 2 + act_rows * l.K * 2 + pairs * R * 4
             out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
     return out
@@ -250,10 +271,20 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------------ our arm
-def kernel_hash() -> str:
+# Sources each recorded kernel is built from; a traffic record holds only while they are unchanged.
+KERNEL_SOURCES = {
+    ("decode", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
+    ("decode", "expand"): ("lora_kernels.cu", "expand_vfull.cuh", "ptx.cuh", "internal.h"),
+    ("prefill", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
+    ("prefill", "shrink"): ("sgmv_tc.cu", "lora_kernels.cu", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_hash(files=None) -> str:
+    """sha256 prefix over the named kernel sources (all of csrc/ when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rank_adapter_gemm_token_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -263,14 +294,14 @@ def recorded_traffic(kind: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json), or None when
     missing or taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or (workload, kind) not in KERNEL_SOURCES:
         return None
     try:
         rec = json.load(open(path))
     except ValueError:
         return None
     r = rec.get(workload, {}).get(kind)
-    if not r or r.get("kernel_hash") != kernel_hash():
+    if not r or r.get("kernel_hash") != kernel_hash(KERNEL_SOURCES[(workload, kind)]):
         return None
     return r.get("dram_bytes_per_launch")
 

@@ -572,6 +572,19 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, long rows, int cols, int
   return make_tmap_bf16_impl(map, base, rows, cols, box_rows, box_cols);
 }
 
+bool make_tmap_f32_sw128(CUtensorMap* map, const void* base, long rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (cols & 3) != 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                                   uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
                                   cudaStream_t s) {
@@ -580,8 +593,14 @@ cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y
     SkinnyShrink none{};
     return launch_skinny(x, W, y, T, K, D, err, num_sms, nullptr, 0, none, s);
   }
-  // Largest N tile that still gives every SM a tile; small problems take N = 64.
+  // Enough 256 x 256 tiles for every CTA pair: the pair kernel. Otherwise the largest one-CTA
+  // N tile that still gives every SM a tile; small problems take N = 64.
   const int m_tiles = (T + BM - 1) / BM;
+  const int forced_n = gemm_tile_n();
+  if (forced_n > 0) return launch_pair_gemm(x, W, y, T, K, D, err, pool, meta, forced_n, s);
+  const int max_pairs = forced_n < 0 ? 0 : pair_gemm_max_pairs();
+  if (max_pairs > 0 && ((m_tiles + 1) / 2) * ((D + 255) / 256) >= max_pairs)
+    return launch_pair_gemm(x, W, y, T, K, D, err, pool, meta, 0, s);
   if (m_tiles * ((D + 255) / 256) >= num_sms)
     return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
   if (m_tiles * ((D + 127) / 128) >= num_sms)

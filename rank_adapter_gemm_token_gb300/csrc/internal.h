@@ -37,7 +37,7 @@ struct MetaView {
   int32_t* blk_start;   // [n]   start of the block inside order
   int32_t* blk_count;   // [n]   pairs in the block
   int32_t* counts;      // [8] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none),
-                        //     n_act (distinct slots with an active pair)
+                        //     n_act (distinct slots with an active pair), n_todo (entries of todo_blk)
   int32_t* pair_act;    // [n] index of the pair's slot among the active slots (-1: none)
   int32_t* act_slot;    // [n] active slots in ascending order
   uint32_t* err;        // device error word (ptx::kErr* bits)
@@ -47,6 +47,7 @@ struct MetaView {
   int32_t* tile_info;   // per 128-token M-tile: [count, slot_0 .. slot_{kTileSlots-1}] (ascending,
                         //   -1 unused); count > kTileSlots = too many slots (overflow tile)
   int32_t* pair_fused;  // [n] 1: the pair's side path runs on the tensor cores inside the GEMM
+  int32_t* todo_blk;    // [n] ascending pair-block numbers holding a pair with pair_fused == 0
   uint16_t* vtile;      // tensor-core shrink output: [tiles][kTileSlots][128][64] bf16, s c v per token
   int n;                // pairs of the current step (T * J)
   int T, J;
@@ -71,6 +72,9 @@ void note_launch_end(int kind, cudaStream_t s);
 // Row-major bf16 matrix [rows, cols] as a TMA tensor map with a box of box_rows x box_cols and
 // the 128-byte swizzle (gemm_tc.cu). False if the encoder is unavailable or rejects it.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, long rows, int cols, int box_rows, int box_cols);
+// Row-major fp32 matrix [rows, cols] with a box of box_rows x 32 columns (128 bytes, 128-byte
+// swizzle), for tiled stores. False unless cols is a multiple of 4 and base 16-byte aligned.
+bool make_tmap_f32_sw128(CUtensorMap* map, const void* base, long rows, int cols, int box_rows);
 
 // Launchers. Each returns the cudaError_t of its launch.
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
@@ -102,6 +106,17 @@ cudaError_t launch_sgmv_shrink_tc(const uint16_t* x, const PoolView& pool, const
 cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                                   uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
                                   cudaStream_t s);
+// CTA-pair (cta_group::2) tiled GEMM for large batches (gemm_pair.cu): 256 x 256 tiles of y on
+// clusters of two CTAs, with the same fused side-path K blocks as the one-CTA tiled GEMM.
+// pair_gemm_max_pairs() = clusters of two that can be resident at once (0: not available).
+// pair_gemm_pick_n() = the N tile (256, 224, 192 or 128) that best fills whole waves; bn = 0 in
+// launch_pair_gemm picks it. gemm_tile_n() is the process-wide choice set by
+// mlora_set_gemm_tile_n (0 automatic, -1 never the pair kernel, else that N tile).
+int pair_gemm_max_pairs();
+int pair_gemm_pick_n(int T, int D, int max_pairs);
+cudaError_t launch_pair_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                             const PoolView* pool, const MetaView* meta, int bn, cudaStream_t s);
+int gemm_tile_n();
 
 // K elements per shrink split and the number of splits for a pool of width R.
 void shrink_split(int K, int R, int* kc_len, int* n_ks);

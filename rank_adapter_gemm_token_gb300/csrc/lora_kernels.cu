@@ -65,19 +65,15 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
   constexpr int V = 8 / RPW;                                  // vectors per lane per row
   ptx::grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int items = m.counts[2] * n_ks;
+  const int items = m.counts[skip_fused ? 5 : 2] * n_ks;       // skip_fused: only todo_blk's blocks
   const int K = pool.K, R = pool.R;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int b = item / n_ks, ks = item - b * n_ks;
+    const int bi = item / n_ks, ks = item - bi * n_ks;
+    const int b = skip_fused ? m.todo_blk[bi] : bi;
     const int slot = m.blk_slot[b];
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
-    if (skip_fused) {                                         // all pairs done on the tensor cores?
-      bool todo = false;
-      for (int i = 0; i < cnt; ++i) todo |= !m.pair_fused[m.order[start + i]];
-      if (!todo) continue;                                    // uniform across the block
-    }
     const int k0 = ks * kc_len;
     const int nv = (min(K, k0 + kc_len) - k0) / 8;            // vectors in this split
     for (int qg = warp; qg < rank; qg += 8 * RPW) {           // rows qg + 8 i, i < RPW
@@ -155,21 +151,17 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
                            int skip_fused) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
-  const int items = m.counts[2] * n_dchunk;
+  const int items = m.counts[skip_fused ? 5 : 2] * n_dchunk;   // skip_fused: only todo_blk's blocks
   const int R = pool.R, D = pool.D;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int b = item / n_dchunk, dc = item - b * n_dchunk;
+    const int bi = item / n_dchunk, dc = item - bi * n_dchunk;
+    const int b = skip_fused ? m.todo_blk[bi] : bi;
     const int slot = m.blk_slot[b];
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
     const float c = pool.slot_scale[slot];
     const int rpad = (rank + 7) & ~7;
-    if (skip_fused) {                                         // all pairs done on the tensor cores?
-      bool todo = false;
-      for (int i = 0; i < cnt; ++i) todo |= !m.pair_fused[m.order[start + i]];
-      if (!todo) continue;                                    // uniform across the block
-    }
     __syncthreads();
     for (int i = threadIdx.x; i < cnt * rpad; i += kExpandThreads) {
       const int pi = i / rpad, q = i - pi * rpad;
@@ -206,7 +198,7 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
   const int J = m.J, R = pool.R, D = pool.D;
-  const int items = m.T * n_dchunk;
+  const int items = (skip_fused && m.counts[5] == 0) ? 0 : m.T * n_dchunk;   // nothing left off the tensor cores
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int t = item / n_dchunk, dc = item - t * n_dchunk;
     bool any = false;

@@ -63,6 +63,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
+  __shared__ int n_blk_sh;                               // pair-blocks in total
   __shared__ int tile_cnt[kMaxTiles];                    // distinct slots per 128-token M-tile
   __shared__ int tile_list[kMaxTiles * kTileSlots];
 
@@ -134,6 +135,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     m.counts[1] = n - hist[0];
     m.counts[2] = pk;
     m.counts[4] = pf - has_sentinel;
+    n_blk_sh = pk;
   }
   __syncthreads();
 
@@ -206,6 +208,27 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __syncthreads();
   for (int p = tid; p < n; p += kMetaThreads)
     m.pair_fused[p] = m.pair_slot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
+
+  // 5. the pair-blocks that still need the CUDA-core shrink/expand (a pair in an overflow tile),
+  //    in ascending order, so those kernels skip the fused blocks without looking at them
+  {
+    auto todo = [&](int b) {
+      const int start = m.blk_start[b], cnt = m.blk_count[b];
+      bool t = false;
+      for (int i = 0; i < cnt; ++i) t |= tile_cnt[(m.order[start + i] / m.J) >> 7] > kTileSlots;
+      return t;
+    };
+    const int nblk = n_blk_sh;
+    const int per_b = (nblk + kMetaThreads - 1) / kMetaThreads;
+    const int c0 = min(tid * per_b, nblk), c1 = min(c0 + per_b, nblk);
+    int mine = 0;
+    for (int b = c0; b < c1; ++b) mine += todo(b);
+    int pos, unused0, unused1;
+    block_exclusive_scan3(mine, 0, 0, pos, unused0, unused1, warp_sums);
+    if (tid == kMetaThreads - 1) m.counts[5] = pos + mine;
+    for (int b = c0; b < c1; ++b)
+      if (todo(b)) m.todo_blk[pos++] = b;
+  }
 
   if (tid == 0) {
     m.counts[3] = first_bad;

@@ -50,6 +50,7 @@ mlora_status cuda_fail(cudaError_t e, const char* what) {
   } while (0)
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_gemm_tile_n{0};          // mlora_set_gemm_tile_n
 
 // ---------------------------------------------------------------- trace
 struct TraceRec {
@@ -107,6 +108,7 @@ namespace mlora {
 
 int report_error(int status, const char* message) { return fail(status, "%s", message); }
 int report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+int gemm_tile_n() { return g_gemm_tile_n.load(std::memory_order_relaxed); }
 
 void note_launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -163,7 +165,7 @@ struct mlora_meta {
   float* vpart = nullptr;
   float* vfull = nullptr;
   int vfull_ld = 0;
-  int32_t *tile_info = nullptr, *pair_fused = nullptr;
+  int32_t *tile_info = nullptr, *pair_fused = nullptr, *todo_blk = nullptr;
   uint16_t* vtile = nullptr;
   int T = 0, J = 1, S = -1;
   bool built = false;
@@ -172,7 +174,7 @@ struct mlora_meta {
 
   MetaView view() const {
     return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count, counts,
-                    pair_act, act_slot, err, vpart, vfull, vfull_ld, tile_info, pair_fused, vtile,
+                    pair_act, act_slot, err, vpart, vfull, vfull_ld, tile_info, pair_fused, todo_blk, vtile,
                     T * J, T, J};
   }
 };
@@ -180,6 +182,13 @@ struct mlora_meta {
 extern "C" {
 
 int mlora_version(void) { return 1; }
+
+mlora_status mlora_set_gemm_tile_n(int n) {
+  if (n != 0 && n != -1 && n != 256 && n != 224 && n != 192 && n != 128)
+    return fail(MLORA_ERR_INVALID_ARG, "tile N must be 0 (automatic), -1 (one-CTA kernel), 256, 224, 192 or 128");
+  g_gemm_tile_n.store(n);
+  return MLORA_OK;
+}
 
 uint64_t mlora_launch_count(void) { return g_launches.load(); }
 
@@ -422,6 +431,7 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   const size_t n_tiles = (static_cast<size_t>(max_tokens) + 127) / 128;
   alloc(reinterpret_cast<void**>(&m->tile_info), n_tiles * (kTileSlots + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->pair_fused), n * 4);
+  alloc(reinterpret_cast<void**>(&m->todo_blk), n * 4);
   alloc(reinterpret_cast<void**>(&m->vtile), n_tiles * kTileSlots * 128 * 64 * 2);
   // small-batch shrink output: v of every token (up to 256) against every active slot
   const int vt = std::min(max_tokens, kVfullMaxTokens);
@@ -463,6 +473,7 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->act_slot);
   cudaFree(m->tile_info);
   cudaFree(m->pair_fused);
+  cudaFree(m->todo_blk);
   cudaFree(m->vtile);
   delete m;
   return MLORA_OK;

@@ -34,7 +34,7 @@ EXPORTS = (
     "mlora_meta_status", "mlora_meta_read", "mlora_linear", "mlora_base_gemm", "mlora_lora_shrink",
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
-    "mlora_lora_apply_noalloc",
+    "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n",
 )
 
 
@@ -83,6 +83,7 @@ def load(path: str | None = None):
             "mlora_trace_disable": [],
             "mlora_trace_read": [i32, vp, vp],
             "mlora_lora_apply_noalloc": [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp],
+            "mlora_set_gemm_tile_n": [i32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -225,6 +226,11 @@ def mlora_lora_apply_noalloc(x, y, token_slots, scales, T: int, J: int, A_pool, 
     _check(load().mlora_lora_apply_noalloc(_ptr(x), _ptr(y), _ptr(token_slots), _ptr(scales), T, J, _ptr(A_pool),
                                            _ptr(B_pool), _ptr(slot_scale), _ptr(slot_rank), n_slots, r_pad, K, D,
                                            _stream(stream)), "mlora_lora_apply_noalloc")
+
+
+def mlora_set_gemm_tile_n(n: int) -> None:
+    """0 automatic, -1 never the CTA-pair GEMM, 256/224/192/128 always it with that N tile."""
+    _check(load().mlora_set_gemm_tile_n(n), "mlora_set_gemm_tile_n")
 
 
 # ------------------------------------------------------------------------- diagnostics

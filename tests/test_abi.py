@@ -97,3 +97,12 @@ def test_missing_library_fails_loudly(tmp_path):
     from rank_adapter_gemm_token_gb300 import mlora
     with pytest.raises(FileNotFoundError):
         mlora.load(str(tmp_path / "libmlora.so"))
+
+
+def test_gemm_tile_choice_is_validated(lib):
+    from rank_adapter_gemm_token_gb300 import mlora
+    for n in (256, 224, 192, 128, -1, 0):
+        assert lib.mlora_set_gemm_tile_n(n) == mlora.MLORA_OK
+    for n in (1, 64, 160, 512, -2):
+        assert lib.mlora_set_gemm_tile_n(n) == mlora.MLORA_ERR_INVALID_ARG
+    assert lib.mlora_set_gemm_tile_n(0) == mlora.MLORA_OK

@@ -26,6 +26,38 @@ def test_small_and_ragged_shapes(cuda_device, T, K, D):
     assert_close(y, ref, f"gemm {T}x{K}x{D}")
 
 
+@pytest.mark.parametrize("T,K,D", [(1900, 328, 2504), (2048, 512, 4864)])
+def test_pair_tile_shapes(cuda_device, T, K, D):
+    # at least 76 tiles of 256 x 256: the CTA-pair kernel; ragged T (odd 128-row tile count), K, D
+    x, W, y = _run(T, K, D, seed=T + K + D)
+    ref = oracle.linear(x, W, np.full((T, 1), -1), {}, 1)
+    assert_close(y, ref, f"gemm {T}x{K}x{D}")
+
+
+@pytest.fixture
+def gemm_tile():
+    from rank_adapter_gemm_token_gb300 import mlora
+    yield mlora.mlora_set_gemm_tile_n
+    mlora.mlora_set_gemm_tile_n(0)
+
+
+@pytest.mark.parametrize("bn,D", [(256, 1000), (224, 1000), (192, 1000), (128, 1000), (-1, 1000),
+                                  (224, 960), (192, 1024)])
+def test_every_gemm_tile_choice(cuda_device, gemm_tile, bn, D):
+    # each N tile of the CTA-pair kernel (and the one-CTA kernel, -1) on ragged shapes; D = 960
+    # (224) and 1024 (192) end in a tile of two real 32-column store boxes followed by boxes past
+    # the edge. Repeated launches must agree bit for bit.
+    from rank_adapter_gemm_token_gb300 import layer
+    gemm_tile(bn)
+    T, K = 1500, 328
+    x, W, y = _run(T, K, D, seed=bn + D)
+    ref = oracle.linear(x, W, np.full((T, 1), -1), {}, 1)
+    assert_close(y, ref, f"gemm {T}x{K}x{D} tile {bn}")
+    xd, Wd = layer.bf16_from_bits(x, "cuda"), layer.bf16_from_bits(W, "cuda")
+    for _ in range(3):
+        assert np.array_equal(layer.base_gemm(xd, Wd).cpu().numpy(), y), "GEMM result differs between launches"
+
+
 @pytest.mark.parametrize("T,K,D", [(256, 4096, 4096), (4096, 4096, 2048), (1024, 14336, 4096)])
 def test_large_shapes_sampled(cuda_device, T, K, D):
     x, W, y = _run(T, K, D, seed=D + K)
@@ -34,11 +66,12 @@ def test_large_shapes_sampled(cuda_device, T, K, D):
     assert_close(y[rows], ref, f"gemm {T}x{K}x{D}")
 
 
-def test_small_integers_are_exact(cuda_device):
-    # Small integers in bf16 give exact fp32 products and sums: the GPU must equal the oracle bit for bit.
+@pytest.mark.parametrize("T,K,D", [(200, 320, 136), (1900, 200, 2600)])
+def test_small_integers_are_exact(cuda_device, T, K, D):
+    # Small integers in bf16 give exact fp32 products and sums: the GPU must equal the oracle bit
+    # for bit (one-CTA skinny kernel; CTA-pair kernel with a ragged last pair tile).
     from rank_adapter_gemm_token_gb300 import layer
     rng = np.random.default_rng(5)
-    T, K, D = 200, 320, 136
     xf = rng.integers(-3, 4, size=(T, K)).astype(np.float32)
     Wf = rng.integers(-3, 4, size=(D, K)).astype(np.float32)
     bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)  # noqa: E731  (exact for small ints)

@@ -224,13 +224,19 @@ def test_clear_slot_makes_it_empty(cuda_device):
     dw.close()
 
 
-@pytest.mark.parametrize("J,seed", [(1, 5), (2, 6)])
-def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed):
+@pytest.mark.parametrize("J,seed,T,K,D,bn", [(1, 5, 700, 320, 392, 0), (2, 6, 700, 320, 392, 0),
+                                              (1, 7, 1900, 328, 2504, 0), (2, 8, 1900, 328, 2504, 0),
+                                              (1, 9, 1900, 328, 2504, 224), (2, 10, 1500, 200, 1000, 128),
+                                              (1, 11, 1500, 200, 1000, 256)])
+def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed, T, K, D, bn):
     """T > 256 with r_max 64: runs of one slot (M-tiles with at most 4 slots: shrink on the tensor
     cores, expand inside the base GEMM) followed by per-token random slots (tiles with more
-    slots: CUDA-core path). Ragged T, K and D; mixed ranks; a second slot per token for J = 2."""
+    slots: CUDA-core path). Ragged T, K and D; mixed ranks; a second slot per token for J = 2.
+    The 1900 x 2504 cases have enough 256 x 256 tiles for the CTA-pair GEMM, an odd number of
+    128-row M-tiles (the last pair tile has one) and pairs of M-tiles with different slot lists."""
     rng = np.random.default_rng(seed)
-    T, K, D, S, R = 700, 320, 392, 12, 64
+    S, R = 12, 64
+    seg_end = 5 * T // 7
     lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
     for s in range(S):
         r = (8, 16, 64, 40)[s % 4]
@@ -239,18 +245,23 @@ def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed):
                                         rank=r, alpha=float(2 * r), rslora=bool(s % 3 == 0))
     slots = np.full((T, J), -1, dtype=np.int32)
     t = 0
-    while t < 500:                                  # segments of one slot (some of them -1)
+    while t < seg_end:                              # segments of one slot (some of them -1)
         n = int(rng.integers(40, 170))
         slots[t:t + n, 0] = int(rng.integers(-1, S))
         t += n
-    slots[500:, 0] = rng.integers(-1, S, size=T - 500)
+    slots[seg_end:, 0] = rng.integers(-1, S, size=T - seg_end)
     if J == 2:
         slots[:, 1] = np.where(rng.uniform(size=T) < 0.5, rng.integers(0, S, size=T), -1)
     scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
     wl = synth.Workload("tc-prefill", seed, T, J, S, R, slots, scales,
                         {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
-    dw = DeviceWorkload(wl)
-    dw.run()
-    dw.meta.status()
-    _check_linear(wl, dw, dw.linears[0])
-    dw.close()
+    from rank_adapter_gemm_token_gb300 import mlora
+    mlora.mlora_set_gemm_tile_n(bn)              # 0: automatic; else the CTA-pair GEMM with this N tile
+    try:
+        dw = DeviceWorkload(wl)
+        dw.run()
+        dw.meta.status()
+        _check_linear(wl, dw, dw.linears[0])
+        dw.close()
+    finally:
+        mlora.mlora_set_gemm_tile_n(0)
