@@ -236,7 +236,15 @@ struct SkinnyShrink {
   int n_ablk;                // A-row blocks in the grid (enough for every possible active slot)
 };
 
+// Tensor maps over the A pool with boxes of R, 2R, 4R, ... rows (up to 128): a run of 2^k active
+// slots with consecutive ids is one box, since their rows are contiguous in the pool.
+constexpr int kABoxMaps = 5;
+struct SkinnyAMaps {
+  CUtensorMap box[kABoxMaps];
+};
+
 constexpr int kSkinnyStages = 4;
+constexpr int kPullLoads = 12;            // distributed-shared-memory loads in flight per thread
 constexpr int kSkinnyABytes = BM * BK * 2;
 constexpr int kSkinnyMaxSplit = 8;
 
@@ -245,9 +253,58 @@ __host__ __device__ constexpr int skinny_smem_bytes(int NT) {
   return kSkinnyStages * skinny_stage_bytes(NT) + 256 + 1024;
 }
 
+// Split-K reduction of the skinny kernel: every CTA of the cluster holds its fp32 partial tile
+// part[t][o] (t < NT, o < 128) in shared memory; this CTA sums, for tokens [t0, t1) and the first
+// `rows` o, the partials of ranks 0 .. SPLIT-1 in that order (deterministic) and stores
+// out[t * ld + o] for o < cols (out = the output rows of this block). Work item = 4 consecutive o
+// of one token; each thread keeps the loads of several items in flight before summing.
+template <int SPLIT>
+__device__ __forceinline__ void skinny_pull(cooperative_groups::cluster_group& cluster, float* part, int t0, int t1,
+                                            int rows, float* out, long ld, int cols) {
+  constexpr int kItems = kPullLoads / SPLIT > 1 ? kPullLoads / SPLIT : 1;
+  const int n_items = (t1 - t0) * (BM / 4);
+  const bool vec = (cols & 3) == 0 && (ld & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  for (int w0 = threadIdx.x; w0 < n_items; w0 += kItems * kGemmThreads) {
+    float4 pv[kItems][SPLIT];
+#pragma unroll
+    for (int h = 0; h < kItems; ++h) {
+      const int w = w0 + h * kGemmThreads;
+      const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
+      if (w < n_items && o4 < rows) {
+#pragma unroll
+        for (int r = 0; r < SPLIT; ++r)
+          pv[h][r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kItems; ++h) {
+      const int w = w0 + h * kGemmThreads;
+      const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
+      if (w >= n_items || o4 >= rows) continue;
+      float4 acc = pv[h][0];
+#pragma unroll
+      for (int r = 1; r < SPLIT; ++r) {
+        acc.x += pv[h][r].x;
+        acc.y += pv[h][r].y;
+        acc.z += pv[h][r].z;
+        acc.w += pv[h][r].w;
+      }
+      float* dst = out + static_cast<size_t>(t) * ld + o4;
+      if (vec && o4 + 4 <= cols) {
+        *reinterpret_cast<float4*>(dst) = acc;
+      } else {
+        if (o4 < cols) dst[0] = acc.x;
+        if (o4 + 1 < cols) dst[1] = acc.y;
+        if (o4 + 2 < cols) dst[2] = acc.z;
+        if (o4 + 3 < cols) dst[3] = acc.w;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                        const __grid_constant__ CUtensorMap tmap_a, float* __restrict__ y, int T, int D, int K,
+                        const __grid_constant__ SkinnyAMaps amaps, float* __restrict__ y, int T, int D, int K,
                         int NT, int splitk, uint32_t tmem_cols, uint32_t* __restrict__ err, SkinnyShrink sh) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
@@ -283,7 +340,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
     ptx::mbar_init(acc_full, 1);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
-    ptx::tma_prefetch_desc(a_blk ? &tmap_a : &tmap_w);
+    ptx::tma_prefetch_desc(a_blk ? &amaps.box[0] : &tmap_w);
     ptx::tma_prefetch_desc(&tmap_x);
   }
   if (warp == 2 && !a_blk)
@@ -308,7 +365,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
       const int n_box = min(spb, n_act - a0);
       for (int e = lane; e < n_box * (kb1 - kb0); e += 32) {
         const int i = e % n_box, kb = kb0 + e / n_box;
-        ptx::tma_prefetch_l2_2d(&tmap_a, kb * BK, sh.act_slot[a0 + i] * sh.R);
+        ptx::tma_prefetch_l2_2d(&amaps.box[0], kb * BK, sh.act_slot[a0 + i] * sh.R);
       }
     }
   }
@@ -318,12 +375,23 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
     // nothing to multiply: only the expand phase below (if any)
   } else if (warp == 0) {
     if (lane == 0) {
-      // A rows of the block: one TMA box per active slot (R rows each) or one W box of 128 rows
-      int slot_row[BM / 8];
-      int n_box = 1;
+      // A rows of the block: the active slots' R rows, one TMA box per run of 2^k slots with
+      // consecutive ids (largest power of two first), or one W box of 128 rows
+      int chunk_row[BM / 8], chunk_pos[BM / 8], chunk_k[BM / 8];
+      int n_box = 1, n_chunk = 0;
       if (a_blk) {
         n_box = min(spb, n_act - a0);
-        for (int i = 0; i < n_box; ++i) slot_row[i] = sh.act_slot[a0 + i] * sh.R;
+        for (int i = 0; i < n_box;) {
+          const int s0 = sh.act_slot[a0 + i];
+          int run = 1;
+          while (i + run < n_box && sh.act_slot[a0 + i + run] == s0 + run) ++run;
+          const int k = 31 - __clz(run);                // 2^k <= run
+          chunk_row[n_chunk] = s0 * sh.R;
+          chunk_pos[n_chunk] = i;
+          chunk_k[n_chunk] = k;
+          ++n_chunk;
+          i += 1 << k;
+        }
       }
       const uint32_t bytes = static_cast<uint32_t>(a_blk ? n_box * sh.R * BK * 2 + NT * BK * 2 : stage_bytes);
       int stage = 0;
@@ -333,8 +401,9 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
         uint8_t* sa = smem + stage * stage_bytes;
         ptx::mbar_arrive_expect_tx(&full[stage], bytes);
         if (a_blk) {
-          for (int i = 0; i < n_box; ++i)
-            ptx::tma_load_2d(sa + i * sh.R * BK * 2, &tmap_a, &full[stage], kb * BK, slot_row[i]);
+          for (int c = 0; c < n_chunk; ++c)
+            ptx::tma_load_2d(sa + chunk_pos[c] * sh.R * BK * 2, &amaps.box[chunk_k[c]], &full[stage], kb * BK,
+                             chunk_row[c]);
         } else {
           ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
         }
@@ -396,45 +465,18 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
     const int per = (T + splitk - 1) / splitk;
     const int t0 = ks * per, t1 = min(T, t0 + per);
     const int rows = a_blk ? min(spb, n_act - a0) * sh.R : BM;
-    const int n_items = (t1 - t0) * (BM / 4);
-    for (int w0 = threadIdx.x; w0 < n_items; w0 += 2 * kGemmThreads) {
-      // two work items per iteration: all their distributed-shared-memory loads are in flight at once
-      float4 pv[2][kSkinnyMaxSplit];
-      bool live[2];
-  #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int w = w0 + h * kGemmThreads;
-        const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
-        live[h] = w < n_items && o4 < rows;
-  #pragma unroll
-        for (int r = 0; r < kSkinnyMaxSplit; ++r)
-          if (live[h] && r < splitk)
-            pv[h][r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
-      }
-  #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!live[h]) continue;
-        const int w = w0 + h * kGemmThreads;
-        const int t = t0 + w / (BM / 4), o4 = (w % (BM / 4)) * 4;
-        float4 acc = pv[h][0];
-  #pragma unroll
-        for (int r = 1; r < kSkinnyMaxSplit; ++r)
-          if (r < splitk) { acc.x += pv[h][r].x; acc.y += pv[h][r].y; acc.z += pv[h][r].z; acc.w += pv[h][r].w; }
-        if (a_blk) {
-          *reinterpret_cast<float4*>(sh.vfull + static_cast<size_t>(t) * sh.vfull_ld + a0 * sh.R + o4) = acc;
-        } else {
-          const int o = o0 + o4;
-          float* dst = y + static_cast<size_t>(t) * D + o;
-          if (o + 4 <= D && (D & 3) == 0) {
-            *reinterpret_cast<float4*>(dst) = acc;
-          } else {
-            if (o < D) dst[0] = acc.x;
-            if (o + 1 < D) dst[1] = acc.y;
-            if (o + 2 < D) dst[2] = acc.z;
-            if (o + 3 < D) dst[3] = acc.w;
-          }
-        }
-      }
+    float* out = a_blk ? sh.vfull + a0 * sh.R : y + o0;
+    const long ld = a_blk ? sh.vfull_ld : D;
+    const int cols = a_blk ? rows : min(BM, D - o0);
+    switch (splitk) {
+      case 1: skinny_pull<1>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 2: skinny_pull<2>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 3: skinny_pull<3>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 4: skinny_pull<4>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 5: skinny_pull<5>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 6: skinny_pull<6>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 7: skinny_pull<7>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      default: skinny_pull<8>(cluster, part, t0, t1, rows, out, ld, cols); break;
     }
     ptx::cluster_sync_all();                          // no CTA leaves while others read its tile
   }
@@ -538,12 +580,16 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap mw, mx, ma;
+  CUtensorMap mw, mx;
+  SkinnyAMaps ma;
   if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
-  if (sh.n_ablk > 0) {
-    if (!make_tmap_bf16_impl(&ma, A_pool, static_cast<long>(S) * sh.R, K, sh.R, BK)) return cudaErrorInvalidValue;
-  } else {
-    ma = mw;
+  for (int k = 0; k < kABoxMaps; ++k) {
+    if (sh.n_ablk > 0 && (sh.R << k) <= BM) {
+      if (!make_tmap_bf16_impl(&ma.box[k], A_pool, static_cast<long>(S) * sh.R, K, sh.R << k, BK))
+        return cudaErrorInvalidValue;
+    } else {
+      ma.box[k] = mw;                                   // never used
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_oblk * splitk, 1, 1);
