@@ -275,7 +275,7 @@ def run_reference(args):
 KERNEL_SOURCES = {
     ("decode", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
     ("decode", "expand"): ("lora_kernels.cu", "expand_vfull.cuh", "ptx.cuh", "internal.h"),
-    ("prefill", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
+    ("prefill", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
     ("prefill", "shrink"): ("sgmv_tc.cu", "lora_kernels.cu", "ptx.cuh", "internal.h"),
 }
 
