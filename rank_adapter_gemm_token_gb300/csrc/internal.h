@@ -100,7 +100,7 @@ cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaV
 bool sgmv_tc_supported(int R);
 // vtile = scaled (x A_slot^T) per (M-tile, slot) for tiles with at most kTileSlots slots.
 cudaError_t launch_sgmv_shrink_tc(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
-                                  cudaStream_t s);
+                                  int num_sms, cudaStream_t s);
 // Tiled base GEMM; with pool and meta it also adds vtile x B_slot^T as extra K blocks of the
 // fused tiles.
 cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,

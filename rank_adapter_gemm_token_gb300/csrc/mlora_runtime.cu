@@ -628,7 +628,7 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   } else if (m->T > kSkinnyMaxT && sgmv_tc_supported(p->R)) {
     // larger batch, rank width 64: tiles whose tokens use few slots get the shrink on the tensor
     // cores and the expand as extra K blocks of the base GEMM; the rest take the CUDA-core path
-    if ((e = launch_sgmv_shrink_tc(x, pv, mv, ds->err, s)) != cudaSuccess) return cuda_fail(e, "SGMV shrink launch");
+    if ((e = launch_sgmv_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "SGMV shrink launch");
     if ((e = launch_base_gemm_lora(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, &pv, &mv, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");
     if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "shrink launch");
