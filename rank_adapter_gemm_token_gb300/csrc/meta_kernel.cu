@@ -21,6 +21,11 @@
 namespace mlora {
 namespace {
 
+// Dynamic shared memory of the metadata kernel: the per-bin arrays (80 B per slot bin, up to
+// 164 KB at 2048 slots) plus, when they fit, four int arrays over the pairs (16 B per pair).
+// The kernel's static arrays (~11 KB) come on top, within the 227 KB a block may use.
+constexpr size_t kMetaMaxDynSmem = 200 * 1024;
+
 __device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& pa, int& pb, int& pc,
                                                       int* warp_sums /* [3][32] */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -53,7 +58,7 @@ __device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& 
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
 build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, int S,
-                  const int32_t* __restrict__ slot_rank, MetaView m) {
+                  const int32_t* __restrict__ slot_rank, MetaView m, int cache) {
   extern __shared__ int smem[];
   const int nb = S + 1;
   int* hist = smem;                          // [nb] pairs per bin
@@ -61,6 +66,13 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   int* chunk_tot = cursor + nb;              // [nb] pairs per bin in the current chunk
   int* actidx = chunk_tot + nb;              // [nb] index among the active slots (-1: none)
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
+  // small steps keep their pair slots, order and pair-blocks in shared memory as well, so the
+  // later steps read them there instead of going back to global memory
+  int* c_base = reinterpret_cast<int*>(wcnt + 32 * nb);
+  int* pslot = cache ? c_base : m.pair_slot;            // [n] validated slot per pair
+  int* ord = cache ? c_base + n : m.order;              // [n] sorted pair order
+  int* bstart = cache ? c_base + 2 * n : m.blk_start;   // [n] pair-block starts
+  int* bcount = cache ? c_base + 3 * n : m.blk_count;   // [n] pair-block sizes
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
   __shared__ int n_blk_sh;                               // pair-blocks in total
@@ -69,6 +81,9 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   ptx::grid_dependents_launch();             // the first linear's GEMM may start its set-up
+  // the first chunk's inputs are loaded while the slot table is staged
+  const int s_first = tid < n ? token_slots[tid] : -1;
+  const float c_first = tid < n && scales ? scales[tid] : 1.0f;
   // 0. which slots hold an adapter (staged once, so pair validation needs no dependent load);
   //    `cursor` is free until step 2
   for (int b = tid; b < nb; b += kMetaThreads) {
@@ -81,14 +96,15 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   // 1. validate, histogram, per-pair slot and scale; the first chunk's bins stay in registers
   int first_bin = nb;
   for (int p = tid; p < n; p += kMetaThreads) {
-    int s = token_slots[p];
+    int s = p < kMetaThreads ? s_first : token_slots[p];
     const bool ok = (s == -1) || (s >= 0 && s < S && cursor[s]);
     if (!ok) {
       atomicMin(&first_bad, p);
       s = -1;
     }
     m.pair_slot[p] = s;
-    m.pair_scale[p] = (s < 0) ? 0.0f : (scales ? scales[p] : 1.0f);
+    if (cache) pslot[p] = s;
+    m.pair_scale[p] = (s < 0) ? 0.0f : (p < kMetaThreads ? c_first : (scales ? scales[p] : 1.0f));
     atomicAdd(&hist[s + 1], 1);
     if (p < kMetaThreads) first_bin = s + 1;
   }
@@ -124,6 +140,10 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
           m.blk_slot[pk] = b - 1;
           m.blk_start[pk] = ph + i * kPairBlock;
           m.blk_count[pk] = min(kPairBlock, c - i * kPairBlock);
+          if (cache) {
+            bstart[pk] = ph + i * kPairBlock;
+            bcount[pk] = min(kPairBlock, c - i * kPairBlock);
+          }
         }
       }
     }
@@ -146,7 +166,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     __syncthreads();
     const int p = base + tid;
     const bool valid = p < n;
-    const int bin = !valid ? nb : (base == 0 ? first_bin : m.pair_slot[p] + 1);   // nb = "no pair"
+    const int bin = !valid ? nb : (base == 0 ? first_bin : pslot[p] + 1);   // nb = "no pair"
     const unsigned peers = __match_any_sync(0xffffffffu, bin);
     const int rank_in_warp = __popc(peers & lt_mask);
     if (valid && lane == __ffs(peers) - 1) wcnt[warp * nb + bin] = static_cast<uint16_t>(__popc(peers));
@@ -162,12 +182,25 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     }
     __syncthreads();
     if (valid) {
-      m.order[cursor[bin] + wcnt[warp * nb + bin] + rank_in_warp] = p;
+      const int pos = cursor[bin] + wcnt[warp * nb + bin] + rank_in_warp;
+      m.order[pos] = p;
+      if (cache) ord[pos] = p;
       m.pair_act[p] = actidx[bin];
     }
     __syncthreads();
     for (int b = tid; b < nb; b += kMetaThreads) cursor[b] += chunk_tot[b];
     __syncthreads();
+  }
+
+  // Steps 4 and 5 serve only the tensor-core prefill path, which batches of at most
+  // kSkinnyMaxT tokens never take (they use the small-batch path or the CUDA-core kernels).
+  if (m.T <= kSkinnyMaxT) {
+    if (tid == 0) {
+      m.counts[3] = first_bad;
+      m.counts[5] = 0;
+      if (first_bad != INT_MAX) atomicOr(m.err, ptx::kErrBadSlot);
+    }
+    return;
   }
 
   // 4. slots of each 128-token M-tile (x order), for the tensor-core prefill path: within a
@@ -177,14 +210,14 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   for (int i = tid; i < n_tiles; i += kMetaThreads) tile_cnt[i] = 0;
   __syncthreads();
   for (int i = tid; i < n; i += kMetaThreads) {
-    const int p = m.order[i];
-    const int s = m.pair_slot[p];
+    const int p = ord[i];
+    const int s = pslot[p];
     if (s < 0) continue;
     const int tile = (p / m.J) >> 7;
     bool first = true;
     if (i > 0) {
-      const int q = m.order[i - 1];
-      first = m.pair_slot[q] != s || ((q / m.J) >> 7) != tile;
+      const int q = ord[i - 1];
+      first = pslot[q] != s || ((q / m.J) >> 7) != tile;
     }
     if (first) {
       const int k = atomicAdd(&tile_cnt[tile], 1);
@@ -207,15 +240,15 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   }
   __syncthreads();
   for (int p = tid; p < n; p += kMetaThreads)
-    m.pair_fused[p] = m.pair_slot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
+    m.pair_fused[p] = pslot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
 
   // 5. the pair-blocks that still need the CUDA-core shrink/expand (a pair in an overflow tile),
   //    in ascending order, so those kernels skip the fused blocks without looking at them
   {
     auto todo = [&](int b) {
-      const int start = m.blk_start[b], cnt = m.blk_count[b];
+      const int start = bstart[b], cnt = bcount[b];
       bool t = false;
-      for (int i = 0; i < cnt; ++i) t |= tile_cnt[(m.order[start + i] / m.J) >> 7] > kTileSlots;
+      for (int i = 0; i < cnt; ++i) t |= tile_cnt[(ord[start + i] / m.J) >> 7] > kTileSlots;
       return t;
     };
     const int nblk = n_blk_sh;
@@ -241,16 +274,19 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
                               const int32_t* slot_rank, const MetaView& m, cudaStream_t s) {
   const int nb = S + 1;
-  const size_t smem = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
+  const int n = T * J;
+  const size_t bins = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
+  const int cache = bins + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
+  const size_t smem = bins + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>((kMaxSlots + 1) * (4 * sizeof(int) + 32 * sizeof(uint16_t))));
+                                         static_cast<int>(kMetaMaxDynSmem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   note_launch_begin(kKindMeta, s);
-  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, T * J, S, slot_rank, m);
+  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, S, slot_rank, m, cache);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindMeta, s);
   return e;
