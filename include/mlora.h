@@ -210,6 +210,15 @@ MLORA_API int mlora_version(void);
 /* Kernels this library has launched in this process (all kinds). */
 MLORA_API uint64_t mlora_launch_count(void);
 
+/* Check of the failure path every kernel's waits rely on (no counterpart on the pages). Runs on
+ * `stream` one kernel whose mbarrier wait can never complete (nothing arrives on it); the wait
+ * gives up after the library's limit (2 s), records the timeout in a device error word reserved
+ * for this check and the kernel returns, leaving the context usable. Synchronises the stream.
+ * Returns MLORA_ERR_DEVICE_TIMEOUT when the wait gave up as designed (the expected result),
+ * MLORA_ERR_MISMATCH if no timeout was recorded, MLORA_ERR_CUDA on a CUDA error. Does not touch
+ * the error word that mlora_meta_status reports. */
+MLORA_API mlora_status mlora_check_wait_timeout(void* stream);
+
 /* Per-kernel CUDA-event trace. While enabled, every kernel launch is bracketed by two events
  * on its own stream (at most `capacity` launches are kept). mlora_trace_read synchronises
  * and returns, for each kernel kind, the number of launches and their summed device time in

@@ -106,6 +106,10 @@ cudaError_t launch_sgmv_shrink_tc(const uint16_t* x, const PoolView& pool, const
 cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                                   uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
                                   cudaStream_t s);
+// One block waiting on an mbarrier nothing arrives on (wait_check.cu): exercises the bounded
+// wait, which sets ptx::kErrWaitTimeout in *err after the limit and returns.
+cudaError_t launch_wait_check(uint32_t* err, cudaStream_t s);
+
 // CTA-pair (cta_group::2) tiled GEMM for large batches (gemm_pair.cu): 256 x 256 tiles of y on
 // clusters of two CTAs, with the same fused side-path K blocks as the one-CTA tiled GEMM.
 // pair_gemm_max_pairs() = clusters of two that can be resident at once (0: not available).

@@ -70,6 +70,7 @@ struct DeviceState {
   bool init = false;
   int num_sms = 0;
   uint32_t* err = nullptr;        // library-wide device error word (timeouts of bounded waits)
+  uint32_t* check_err = nullptr;  // error word of mlora_check_wait_timeout only
 };
 DeviceState g_dev[64];
 std::mutex g_dev_mu;
@@ -84,6 +85,7 @@ mlora_status device_state(DeviceState** out) {
     MLORA_CUDA(cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
     MLORA_CUDA(cudaMalloc(&d.err, sizeof(uint32_t)), "cudaMalloc(error word)");
     MLORA_CUDA(cudaMemset(d.err, 0, sizeof(uint32_t)), "cudaMemset(error word)");
+    MLORA_CUDA(cudaMalloc(&d.check_err, sizeof(uint32_t)), "cudaMalloc(check error word)");
     d.init = true;
   }
   *out = &d;
@@ -182,6 +184,19 @@ struct mlora_meta {
 extern "C" {
 
 int mlora_version(void) { return 1; }
+
+mlora_status mlora_check_wait_timeout(void* stream) {
+  DeviceState* ds = nullptr;
+  if (mlora_status st = device_state(&ds)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  MLORA_CUDA(cudaMemsetAsync(ds->check_err, 0, sizeof(uint32_t), s), "clear check error word");
+  MLORA_CUDA(launch_wait_check(ds->check_err, s), "wait-check launch");
+  MLORA_CUDA(cudaMemcpyAsync(&word, ds->check_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s), "read check word");
+  MLORA_CUDA(cudaStreamSynchronize(s), "wait-check sync");
+  if (word & ptx::kErrWaitTimeout) return fail(MLORA_ERR_DEVICE_TIMEOUT, "the check kernel's wait gave up, as designed");
+  return fail(MLORA_ERR_MISMATCH, "the check kernel's wait did not report a timeout (error word %u)", word);
+}
 
 mlora_status mlora_set_gemm_tile_n(int n) {
   if (n != 0 && n != -1 && n != 256 && n != 224 && n != 192 && n != 128)

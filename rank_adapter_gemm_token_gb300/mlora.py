@@ -34,7 +34,7 @@ EXPORTS = (
     "mlora_meta_status", "mlora_meta_read", "mlora_linear", "mlora_base_gemm", "mlora_lora_shrink",
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
-    "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n",
+    "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n", "mlora_check_wait_timeout",
 )
 
 
@@ -84,6 +84,7 @@ def load(path: str | None = None):
             "mlora_trace_read": [i32, vp, vp],
             "mlora_lora_apply_noalloc": [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp],
             "mlora_set_gemm_tile_n": [i32],
+            "mlora_check_wait_timeout": [vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -234,6 +235,11 @@ def mlora_set_gemm_tile_n(n: int) -> None:
 
 
 # ------------------------------------------------------------------------- diagnostics
+def mlora_check_wait_timeout(stream=None) -> int:
+    """Status of the bounded-wait check (MLORA_ERR_DEVICE_TIMEOUT is the expected result)."""
+    return int(load().mlora_check_wait_timeout(_stream(stream)))
+
+
 def mlora_status_string(status: int) -> str:
     return load().mlora_status_string(status).decode()
 
