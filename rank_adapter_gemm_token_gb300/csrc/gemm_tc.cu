@@ -234,6 +234,7 @@ struct SkinnyShrink {
   int vfull_ld;
   int R;                     // rows per slot in the A pool (multiple of 8, divides 128)
   int n_ablk;                // A-row blocks in the grid (enough for every possible active slot)
+  int window;                // 1: shrink only, for the tokens of the step's overflow tiles (below)
 };
 
 // Tensor maps over the A pool with boxes of R, 2R, 4R, ... rows (up to 128): a run of 2^k active
@@ -361,6 +362,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   if (a_blk) {
     n_act = *sh.n_act;
     idle = a0 >= n_act;                                 // uniform across the cluster
+    if (sh.window) idle = idle || sh.meta.counts[6] < 0;   // no window this step: nothing to do
     if (!idle && warp == 2) {                           // this block's adapter rows into L2
       const int n_box = min(spb, n_act - a0);
       for (int e = lane; e < n_box * (kb1 - kb0); e += 32) {
@@ -394,6 +396,9 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
         }
       }
       const uint32_t bytes = static_cast<uint32_t>(a_blk ? n_box * sh.R * BK * 2 + NT * BK * 2 : stage_bytes);
+      // window rows: tile counts[6] and, if present, tile counts[7] (else rows past x: zero fill)
+      const int win_row0 = sh.window ? sh.meta.counts[6] * BM : 0;
+      const int win_row1 = sh.window ? (sh.meta.counts[7] >= 0 ? sh.meta.counts[7] * BM : sh.meta.T + BM) : 0;
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -407,7 +412,12 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
         } else {
           ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
         }
-        ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
+        if (sh.window) {                                // the window's two 128-token tiles (an absent
+          ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, win_row0);   // one reads
+          ptx::tma_load_2d(sa + kSkinnyABytes + BM * BK * 2, &tmap_x, &full[stage], kb * BK, win_row1);  // zeros)
+        } else {
+          ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
+        }
         if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -565,7 +575,8 @@ int skinny_splitk(int n_oblk, int K, int num_sms) {
 
 cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                           int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
-  const int NT = (T + 15) / 16 * 16;
+  // window mode: the tokens are two 128-row tiles of x (256 rows of v), chosen on the device
+  const int NT = sh.window ? 2 * BM : (T + 15) / 16 * 16;
   const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
   const int splitk = skinny_splitk(n_oblk, K, num_sms);
   uint32_t tmem_cols = 32;
@@ -582,7 +593,12 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   }
   CUtensorMap mw, mx;
   SkinnyAMaps ma;
-  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) return cudaErrorInvalidValue;
+  if (sh.window) {
+    if (!make_tmap_bf16_impl(&mx, x, T, K, BM, BK)) return cudaErrorInvalidValue;
+    mw = mx;                                            // no W blocks
+  } else if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) {
+    return cudaErrorInvalidValue;
+  }
   for (int k = 0; k < kABoxMaps; ++k) {
     if (sh.n_ablk > 0 && (sh.R << k) <= BM) {
       if (!make_tmap_bf16_impl(&ma.box[k], A_pool, static_cast<long>(S) * sh.R, K, sh.R << k, BK))
@@ -605,10 +621,10 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  note_launch_begin(kKindGemm, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, T, D, K, NT, splitk, tmem_cols,
-                                     err, sh);
-  note_launch_end(kKindGemm, s);
+  note_launch_begin(sh.window ? kKindShrink : kKindGemm, s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, sh.window ? NT : T, D, K, NT,
+                                     splitk, tmem_cols, err, sh);
+  note_launch_end(sh.window ? kKindShrink : kKindGemm, s);
   return e;
 }
 
@@ -676,8 +692,22 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
   const int max_act = std::min(pool.S, m.n);
   const int n_dchunk = (pool.D + kExpandVfullCols - 1) / kExpandVfullCols;
   SkinnyShrink sh{pool, m, n_dchunk, m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R,
-                  (max_act * pool.R + BM - 1) / BM};
+                  (max_act * pool.R + BM - 1) / BM, 0};
   return launch_skinny(x, W, y, m.T, pool.K, pool.D, err, num_sms, pool.A, pool.S, sh, s);
+}
+
+bool window_shrink_supported(int T, int J, int S, int R, int vfull_ld, int vfull_rows) {
+  if (T <= kSkinnyMaxT || vfull_rows < kSkinnyMaxT) return false;
+  if (R < 8 || R > BM || BM % R != 0) return false;
+  return std::min(S, T * J) * R <= vfull_ld;
+}
+
+cudaError_t launch_gemm_shrink_window(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
+                                      int num_sms, cudaStream_t s) {
+  const int max_act = std::min(pool.S, m.n);
+  SkinnyShrink sh{pool, m, 0, m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R,
+                  (max_act * pool.R + BM - 1) / BM, 1};
+  return launch_skinny(x, nullptr, nullptr, m.T, pool.K, 0, err, num_sms, pool.A, pool.S, sh, s);
 }
 
 }  // namespace mlora

@@ -96,6 +96,17 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
 cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
                                      cudaStream_t s);
 
+// Overflow window of a large batch (T > kSkinnyMaxT): when the step has one or two 128-token tiles
+// with more than kTileSlots slots (the metadata names them in counts[6], counts[7]; counts[6] is
+// -1 otherwise), their pairs take the small-batch machinery: the skinny kernel in shrink-only
+// mode over those 256 token rows (vfull row w = window row), then the vfull expand restricted to
+// the pairs not handled on the tensor cores. Both kernels do nothing when there is no window.
+bool window_shrink_supported(int T, int J, int S, int R, int vfull_ld, int vfull_rows);
+cudaError_t launch_gemm_shrink_window(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
+                                      int num_sms, cudaStream_t s);
+cudaError_t launch_lora_expand_window(float* y, const PoolView& pool, const MetaView& m, int num_sms,
+                                      cudaStream_t s);
+
 // Tensor-core prefill path (sgmv_tc.cu): pools with padded rank R == 64.
 bool sgmv_tc_supported(int R);
 // vtile = scaled (x A_slot^T) per (M-tile, slot) for tiles with at most kTileSlots slots.
@@ -124,10 +135,12 @@ int gemm_tile_n();
 
 // K elements per shrink split and the number of splits for a pool of width R.
 void shrink_split(int K, int R, int* kc_len, int* n_ks);
-// CUDA-core shrink / expand; with skip_fused they leave out the pairs the tensor-core path handles.
+// CUDA-core shrink / expand; with skip_fused they leave out the pairs the tensor-core path handles,
+// and with window they also do nothing when the overflow-window kernels took the step's
+// remaining pairs (counts[6] >= 0).
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s, bool skip_fused = false);
+                               cudaStream_t s, bool skip_fused = false, bool window = false);
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
-                               bool skip_fused = false);
+                               bool skip_fused = false, bool window = false);
 
 }  // namespace mlora

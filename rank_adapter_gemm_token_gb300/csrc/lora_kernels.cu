@@ -65,7 +65,8 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
   constexpr int V = 8 / RPW;                                  // vectors per lane per row
   ptx::grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int items = m.counts[skip_fused ? 5 : 2] * n_ks;       // skip_fused: only todo_blk's blocks
+  // skip_fused bit 1: the overflow-window kernels took the remaining pairs if there is a window
+  const int items = ((skip_fused & 2) && m.counts[6] >= 0) ? 0 : m.counts[skip_fused ? 5 : 2] * n_ks;
   const int K = pool.K, R = pool.R;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int bi = item / n_ks, ks = item - bi * n_ks;
@@ -151,7 +152,8 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
                            int skip_fused) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
-  const int items = m.counts[skip_fused ? 5 : 2] * n_dchunk;   // skip_fused: only todo_blk's blocks
+  // skip_fused: only todo_blk's blocks; bit 1: nothing when the overflow-window kernels ran
+  const int items = ((skip_fused & 2) && m.counts[6] >= 0) ? 0 : m.counts[skip_fused ? 5 : 2] * n_dchunk;
   const int R = pool.R, D = pool.D;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int bi = item / n_dchunk, dc = item - bi * n_dchunk;
@@ -198,7 +200,8 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
   const int J = m.J, R = pool.R, D = pool.D;
-  const int items = (skip_fused && m.counts[5] == 0) ? 0 : m.T * n_dchunk;   // nothing left off the tensor cores
+  const bool none = skip_fused && (m.counts[5] == 0 || ((skip_fused & 2) && m.counts[6] >= 0));
+  const int items = none ? 0 : m.T * n_dchunk;          // nothing left off the tensor cores
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int t = item / n_dchunk, dc = item - t * n_dchunk;
     bool any = false;
@@ -280,7 +283,8 @@ void shrink_split(int K, int R, int* kc_len, int* n_ks) {
 }
 
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s, bool skip_fused) {
+                               cudaStream_t s, bool skip_fused, bool window) {
+  const int skip = skip_fused ? (window ? 3 : 1) : 0;
   if (m.n == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
@@ -289,10 +293,10 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindShrink, s);
   switch (shrink_rows_per_warp(pool.R)) {
-    case 1: lora_shrink_kernel<1><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
-    case 2: lora_shrink_kernel<2><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
-    case 4: lora_shrink_kernel<4><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
-    default: lora_shrink_kernel<8><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip_fused); break;
+    case 1: lora_shrink_kernel<1><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip); break;
+    case 2: lora_shrink_kernel<2><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip); break;
+    case 4: lora_shrink_kernel<4><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip); break;
+    default: lora_shrink_kernel<8><<<grid, kShrinkThreads, 0, s>>>(x, pool, m, kc, n_ks, skip); break;
   }
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindShrink, s);
@@ -300,7 +304,8 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
 }
 
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
-                               bool skip_fused) {
+                               bool skip_fused, bool window) {
+  const int skip = skip_fused ? (window ? 3 : 1) : 0;
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
@@ -310,9 +315,9 @@ cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindExpand, s);
   if (m.J == 1)
-    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip_fused);
+    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip);
   else
-    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip_fused);
+    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindExpand, s);
   return e;

@@ -76,6 +76,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
   __shared__ int n_blk_sh;                               // pair-blocks in total
+  __shared__ int ovf_n, ovf_a, ovf_b;                    // overflow tiles: count, first two
   __shared__ int tile_cnt[kMaxTiles];                    // distinct slots per 128-token M-tile
   __shared__ int tile_list[kMaxTiles * kTileSlots];
 
@@ -198,6 +199,8 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     if (tid == 0) {
       m.counts[3] = first_bad;
       m.counts[5] = 0;
+      m.counts[6] = -1;
+      m.counts[7] = -1;
       if (first_bad != INT_MAX) atomicOr(m.err, ptx::kErrBadSlot);
     }
     return;
@@ -241,6 +244,29 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __syncthreads();
   for (int p = tid; p < n; p += kMetaThreads)
     m.pair_fused[p] = pslot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
+
+  // the overflow window: with one or two overflow tiles, counts[6] and counts[7] name them in
+  // ascending order (counts[7] = -1 for one); otherwise both are -1 (none, or too many)
+  if (tid == 0) {
+    ovf_n = 0;
+    ovf_a = INT_MAX;
+    ovf_b = INT_MAX;
+  }
+  __syncthreads();
+  for (int tile = tid; tile < n_tiles; tile += kMetaThreads)
+    if (tile_cnt[tile] > kTileSlots) {
+      atomicAdd(&ovf_n, 1);
+      atomicMin(&ovf_a, tile);
+    }
+  __syncthreads();
+  for (int tile = tid; tile < n_tiles; tile += kMetaThreads)
+    if (tile_cnt[tile] > kTileSlots && tile != ovf_a) atomicMin(&ovf_b, tile);
+  __syncthreads();
+  if (tid == 0) {
+    const bool win = ovf_n == 1 || ovf_n == 2;
+    m.counts[6] = win ? ovf_a : -1;
+    m.counts[7] = win && ovf_n == 2 ? ovf_b : -1;
+  }
 
   // 5. the pair-blocks that still need the CUDA-core shrink/expand (a pair in an overflow tile),
   //    in ascending order, so those kernels skip the fused blocks without looking at them

@@ -646,8 +646,21 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
     if ((e = launch_sgmv_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "SGMV shrink launch");
     if ((e = launch_base_gemm_lora(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, &pv, &mv, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");
-    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "shrink launch");
-    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "expand launch");
+    // one or two overflow tiles (decode-like tokens of a mixed batch): the small-batch shrink and
+    // expand over those tokens; more overflow tiles: the CUDA-core kernels (each kind does
+    // nothing when the other one applies)
+    const bool win = window_shrink_supported(m->T, m->J, p->S, p->R, m->vfull_ld,
+                                             std::min(m->max_tokens, kVfullMaxTokens));
+    if (win) {
+      if ((e = launch_gemm_shrink_window(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "window shrink launch");
+      if ((e = launch_lora_expand_window(y, pv, mv, ds->num_sms, s)) != cudaSuccess)
+        return cuda_fail(e, "window expand launch");
+    }
+    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true, win)) != cudaSuccess)
+      return cuda_fail(e, "shrink launch");
+    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true, win)) != cudaSuccess)
+      return cuda_fail(e, "expand launch");
   } else {
     if ((e = launch_base_gemm(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");

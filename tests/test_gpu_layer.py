@@ -265,3 +265,38 @@ def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed, T, K
         dw.close()
     finally:
         mlora.mlora_set_gemm_tile_n(0)
+
+
+@pytest.mark.parametrize("J,seed,T,ovf", [(1, 50, 700, (4, 5)), (2, 51, 700, (4, 5)), (1, 52, 900, (1, 5)),
+                                          (1, 53, 640, (2,)), (2, 54, 1100, (0, 8))])
+def test_overflow_window(cuda_device, J, seed, T, ovf):
+    """T > 256, rank width 64: the tiles listed in ovf draw a slot per token from 40 adapters
+    (more than 4 slots per tile: the overflow window, handled by the small-batch shrink and
+    expand over those 256 tokens), the others use runs of one slot (tensor-core path). Covers
+    one and two window tiles, adjacent or not, a ragged last tile, and J = 2."""
+    rng = np.random.default_rng(seed)
+    K, D, S, R = 320, 392, 40, 64
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = (8, 16, 64, 40)[s % 4]
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(seed, 300 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(2 * r), rslora=bool(s % 3 == 0))
+    slots = np.full((T, J), -1, dtype=np.int32)
+    for t0 in range(0, T, 128):
+        t1 = min(T, t0 + 128)
+        if t0 // 128 in ovf:
+            slots[t0:t1, 0] = rng.integers(-1, S, size=t1 - t0)
+            if J == 2:
+                slots[t0:t1, 1] = np.where(rng.uniform(size=t1 - t0) < 0.5, rng.integers(0, S, size=t1 - t0), -1)
+        else:
+            slots[t0:t0 + 70, 0] = int(rng.integers(0, S))
+            slots[t0 + 70:t1, 0] = int(rng.integers(-1, S))
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("overflow-window", seed, T, J, S, R, slots, scales,
+                        {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
+    dw.close()
