@@ -317,6 +317,14 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   float* part = reinterpret_cast<float*>(smem);          // [NT][128] after the main loop
 
+  // window mode without a window this step: the metadata (built before the large-batch GEMM
+  // that precedes this kernel) says so, and the whole grid leaves at once, after the wait that
+  // keeps the launch order of later kernels
+  if (sh.window && sh.meta.counts[6] < 0) {
+    ptx::grid_dependency_wait();
+    ptx::grid_dependents_launch();
+    return;
+  }
   cg::cluster_group cluster = cg::this_cluster();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
