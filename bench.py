@@ -75,6 +75,8 @@ def make_workload(name: str):
         return synth.tiny()
     if name == "prefill":
         return synth.prefill()
+    if name == "mixed":
+        return synth.mixed()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -82,7 +84,8 @@ def workload_config(wl, name: str) -> dict:
     lin = wl.linears
     return {
         "workload": f"{name}: T={wl.T} tokens, J={wl.J}, linears "
-                    + ", ".join(f"{l.name} {l.K}->{l.D}" for l in lin)
+                    + (", ".join(f"{l.name} {l.K}->{l.D}" for l in lin) if len(lin) <= 8 else
+                       f"{len(lin) // 4} layers x (" + ", ".join(f"{l.name.split('.')[-1]} {l.K}->{l.D}" for l in lin[:4]) + ")")
                     + f", {wl.n_slots} slots r_max={wl.r_max}",
         "tokens_per_step": wl.T,
         "linears": len(lin),
@@ -222,6 +225,17 @@ def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
     import oracle
     threads = oracle.default_threads()
     T = wl.T
+    # a step whose tensors are generated on demand (the mixed step): time its first layer and
+    # scale to all layers (every layer has the same shapes and adapter set)
+    scale = 1.0
+    if any(l.W is None for l in wl.linears):
+        first = wl.linears[:len(synth_modules())]
+        scale = len(wl.linears) / len(first)
+        if getattr(wl, "_first_layer", None) is None:     # generated once per workload object
+            wl._first_layer = type(wl)(wl.name, wl.seed, wl.T, wl.J, wl.n_slots, wl.r_max, wl.token_slots,
+                                       wl.scales, {l.x_id: synth_x(wl, l) for l in first},
+                                       [synth_materialize(wl, l) for l in first])
+        wl = wl._first_layer
     cap = T if max_rows is None else min(T, max_rows)
     rows_n = min(cap, max(1, threads))
     spent, tokens = 0.0, 0
@@ -232,14 +246,37 @@ def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
         for l in wl.linears:
             oracle.linear(wl.xs[l.x_id], l.W, wl.token_slots, l.adapters, wl.n_slots, scales=wl.scales,
                           rows=rows, threads=threads)
-        dt = time.perf_counter() - t0
-        spent += dt
+        real = time.perf_counter() - t0
+        spent += real
         tokens = rows_n
-        last = dt
-        if rows_n >= cap or spent + dt * 2.5 > budget_s:
+        last = real * scale
+        if rows_n >= cap or spent + real * 2.5 > budget_s:
             break
         rows_n = min(cap, rows_n * 2)
     return tokens / last, tokens, threads, last
+
+
+def synth_modules():
+    import synth
+    return synth.MIXED_MODULES
+
+
+def synth_x(wl, lin):
+    import synth
+    return synth.materialize_x(wl, lin)
+
+
+def synth_materialize(wl, lin):
+    import synth
+    return synth.materialize_linear(wl, lin)
+
+
+def sample_note(wl, rows, seconds=None) -> str:
+    lazy = any(l.W is None for l in wl.linears)
+    what = (f"{rows} of {wl.T} token rows through the first {len(synth_modules())} of {len(wl.linears)} "
+            f"linears, time scaled to all of them" if lazy else
+            f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears")
+    return what + (f" ({seconds:.1f} s)" if seconds is not None else " per step")
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -263,7 +300,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
         "config": workload_config(wl, args.workload),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears per step"},
+                         "sample": sample_note(wl, rows)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -384,7 +421,7 @@ def run_ours(args):
 
     # ---- per-kernel durations: the same K steps again with the library's event trace
     trace_steps = min(args.steps, 100)
-    mlora.mlora_trace_enable(64 * trace_steps + 64)
+    mlora.mlora_trace_enable(int(kernels_per_step) * trace_steps + 64)
     for i in range(trace_steps):
         flush.zero_()
         dw.run(stream)
@@ -467,7 +504,7 @@ def run_ours(args):
     if ws == 1 and not args.no_cpu_baseline:
         tps, rows, threads, dt = oracle_sample(wl, budget_s=args.cpu_budget)
         cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears ({dt:.1f} s)"}
+               "sample": sample_note(wl, rows, dt)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -498,7 +535,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny", "mixed"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the library directly for every step")

@@ -303,3 +303,65 @@ def mixed_weight_rows(seed: int, layer: int, module: int, K: int, row0: int, n_r
 
 def mixed_x(seed: int, layer: int, module: int, T: int, K: int) -> np.ndarray:
     return normal_bf16(seed, tensor_key(_NS_X, layer, module), (T, K), 1.0)
+
+
+@dataclass
+class LazyAdapter:
+    """An adapter of the mixed step known by its id; A and B are generated on demand."""
+    seed: int
+    layer: int
+    module: int
+    adapter_id: int
+    rank: int
+    alpha: float
+    rslora: bool = False
+
+    def materialize(self, K: int, D: int) -> Adapter:
+        return mixed_adapter(self.seed, self.layer, self.module, self.adapter_id, K, D)
+
+
+def mixed(n_layers: int = 32) -> Workload:
+    """The mixed serving step as a workload whose tensors are generated on demand: linears
+    layer-major over MIXED_MODULES (x_id = linear index), adapters as LazyAdapter, W = None and
+    no xs entries (see materialize_linear / materialize_x)."""
+    plan = mixed_step_plan()
+    seed = plan["seed"]
+    linears = []
+    for l in range(n_layers):
+        for m, (name, K, D, _) in enumerate(MIXED_MODULES):
+            lin = Linear(f"L{l}.{name}", K, D, None, len(linears))
+            for a, s in plan["slot_of"].items():
+                r = plan["rank_of"][a]
+                lin.adapters[s] = LazyAdapter(seed, l, m, a, r, 2.0 * r, False)
+            linears.append(lin)
+    return Workload("mixed", seed, plan["T"], 1, 128, 64, plan["token_slots"], None, {}, linears,
+                    notes="tensors generated on demand by layer and module")
+
+
+def _layer_module(wl: Workload, lin: Linear) -> tuple:
+    return lin.x_id // len(MIXED_MODULES), lin.x_id % len(MIXED_MODULES)
+
+
+def materialize_linear(wl: Workload, lin: Linear) -> Linear:
+    """lin with W and its adapters generated (a no-op for an eager linear)."""
+    if lin.W is not None:
+        return lin
+    l, m = _layer_module(wl, lin)
+    out = Linear(lin.name, lin.K, lin.D, mixed_weight_rows(wl.seed, l, m, lin.K, 0, lin.D), lin.x_id)
+    out.adapters = {s: a.materialize(lin.K, lin.D) for s, a in lin.adapters.items()}
+    return out
+
+
+def materialize_x(wl: Workload, lin: Linear) -> np.ndarray:
+    if lin.x_id in wl.xs:
+        return wl.xs[lin.x_id]
+    l, m = _layer_module(wl, lin)
+    return mixed_x(wl.seed, l, m, wl.T, lin.K)
+
+
+def linear_weight(wl: Workload, lin: Linear) -> np.ndarray:
+    """W of a linear, generated on demand for the mixed step."""
+    if lin.W is not None:
+        return lin.W
+    l, m = _layer_module(wl, lin)
+    return mixed_weight_rows(wl.seed, l, m, lin.K, 0, lin.D)

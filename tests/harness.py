@@ -53,10 +53,17 @@ class DeviceWorkload:
         self.x = {k: layer.bf16_from_bits(v, self.device) for k, v in wl.xs.items()}
         self.linears = []
         for lin in (wl.linears if linears is None else linears):
+            lazy = lin.W is None                  # the mixed step: tensors generated here, per linear
             pool = layer.AdapterPool(wl.n_slots, wl.r_max, lin.K, lin.D)
             for s, ad in lin.adapters.items():
+                if isinstance(ad, synth.LazyAdapter):
+                    ad = ad.materialize(lin.K, lin.D)
                 pool.load(s, ad.A, ad.B, ad.rank, ad.alpha, ad.rslora)
-            W = layer.bf16_from_bits(lin.W, self.device)
+            if lazy:
+                pool.sync()                       # release the pinned staging copies now
+            W = layer.bf16_from_bits(synth.linear_weight(wl, lin), self.device)
+            if lin.x_id not in self.x:
+                self.x[lin.x_id] = layer.bf16_from_bits(synth.materialize_x(wl, lin), self.device)
             y = torch.empty((wl.T, lin.D), dtype=torch.float32, device=self.device)
             self.linears.append(DeviceLinear(lin, pool, W, y))
         for dl in self.linears:
