@@ -1,6 +1,7 @@
 // Expand work items after the small-batch fused GEMM, which leaves v of every token against every
-// active slot in MetaView::vfull. Used by the standalone expand kernels (programmatic dependents
-// of the GEMM) and by the GEMM kernel itself when it runs the expand behind a grid barrier.
+// active slot in MetaView::vfull. Used by the vfull expand kernels (programmatic dependents of
+// the GEMM); the B-row prefetch helper is also called by the GEMM's epilogue warps, and the
+// overflow-window expand (expand_window.cu) shares the shared-memory layout and dot product.
 //
 // y[t][o] += sum_j s c sum_q B_slot[o][q] v[t][slot][q]  ("Multi-LoRA Serving Explained", batched
 // serving: each token's side path added to the shared base product; "[RFC] Per-request
