@@ -70,6 +70,7 @@ enum {
 #define MLORA_MAX_RANK 256
 #define MLORA_MAX_SLOTS_PER_TOKEN 8
 #define MLORA_MAX_TOKENS 65535
+#define MLORA_MAX_SLICES 8            /* output slices of one fused linear (mlora_load_adapter_sliced) */
 
 /* ------------------------------------------------------------------ adapter pool ----- */
 
@@ -98,6 +99,25 @@ MLORA_API mlora_status mlora_pool_destroy(mlora_pool_t pool);
  * With pageable buffers the copy is complete on return. */
 MLORA_API mlora_status mlora_load_adapter(mlora_pool_t pool, int slot, const mlora_bf16* A_host, const mlora_bf16* B_host,
                                 int rank, float alpha, int rslora);
+
+/* Per-slice adapter of a fused linear (qkv, gate_up): the D output columns are n_slices
+ * consecutive slices of widths[i] columns (sum = D), and slice i has its own A_i [rank, K] and
+ * B_i [widths[i], rank] (host bf16, row-major), all of one adapter config (rank, alpha, rslora):
+ *   y[t, off_i .. off_i + widths[i]) += s c B_i (A_i x[t]),  c = alpha / rank (alpha / sqrt(rank)),
+ * off_i = the sum of the earlier widths ("LoRA Serving" (vLLM learning book, ch. 09-04), section 7:
+ * the merged QKV / merged column linear handles each sub-projection's adapter separately; "[vLLM]
+ * LoRA" (secrett2633 blog), layer-implementation section: merged QKV / merged column variants). The slot stores it as one adapter of rank
+ * n_slices * rank: A = [A_1; ...; A_n] and B block-diagonal (slice i's rows hold B_i in columns
+ * i*rank .. and zeros elsewhere), with factor c; the layer kernels run unchanged and each output
+ * slice gets exactly its own side path (the other blocks add exact zeros).
+ * n_slices in [1, MLORA_MAX_SLICES], n_slices * rank <= r_max (else MLORA_ERR_RANK_TOO_LARGE),
+ * widths > 0 and adding up to D (else MLORA_ERR_INVALID_ARG). Ordering, asynchrony and buffer
+ * lifetime as for mlora_load_adapter. */
+MLORA_API mlora_status mlora_load_adapter_sliced(mlora_pool_t pool, int slot, int n_slices, const int* widths,
+                                                 const mlora_bf16* const* A_slices,
+                                                 const mlora_bf16* const* B_slices, int rank, float alpha,
+                                                 int rslora);
+
 
 /* Zeroes a slot and marks it empty (tokens naming it are then rejected). */
 MLORA_API mlora_status mlora_clear_slot(mlora_pool_t pool, int slot);

@@ -5,12 +5,14 @@ leg may import this package; the library (``rank_adapter_gemm_token_gb300``) nev
 and nothing here imports the library. The two share no code.
 
 - ``linear``: the layer's output in fp64 (plain C loops in ``mlora_oracle.c``).
+- ``linear_sliced``: a fused linear whose output slices each have their own adapter.
 - ``meta``: the per-step slot metadata (stable sort of token/slot pairs by slot).
 - ``memory``: the adapter/slot memory arithmetic from the pages.
 
 Parity pins (tests/test_oracle.py) tie each function to the pages: a hand-worked
 example, the merge identity, the PEFT "cat" merge, linearity in the scale, the
-sentinel rows, the printed segment counts and the printed memory figures.
+sentinel rows, the printed segment counts and the printed memory figures; the sliced
+form against the block-diagonal single-adapter identity.
 """
 from __future__ import annotations
 
@@ -134,3 +136,21 @@ def linear(x, W, token_slots, adapters, n_slots: int, scales=None, rows=None, co
     if rc != ORACLE_OK:
         raise OracleError(rc)
     return y
+
+
+def linear_sliced(x, W, token_slots, adapters, n_slots: int, widths, scales=None, rows=None,
+                  threads: int | None = None) -> np.ndarray:
+    """A fused linear (merged qkv / gate_up) whose D = sum(widths) outputs are consecutive slices,
+    each with its own adapter ("LoRA Serving" (vLLM learning book, ch. 09-04), section 7: the merged
+    column linear applies each sub-projection's adapter separately). adapters: slot -> list with one
+    adapter object per slice (A [r, K], B [widths[i], r], rank, alpha, rslora). Each slice is
+    computed as its own linear: W rows of the slice with that slice's adapters."""
+    W = np.asarray(W)
+    out, off = [], 0
+    for i, w in enumerate(widths):
+        ad_i = {s: a[i] for s, a in (adapters or {}).items()}
+        out.append(linear(x, W[off:off + w], token_slots, ad_i, n_slots, scales=scales, rows=rows,
+                          threads=threads))
+        off += w
+    assert off == W.shape[0]
+    return np.concatenate(out, axis=1)

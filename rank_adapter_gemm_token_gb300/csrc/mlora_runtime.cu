@@ -96,10 +96,12 @@ int pad8(int r) { return (r + 7) / 8 * 8; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// rank: rows of A in use (the kernels' bound); scale_rank: the r of the factor (the same for a
+// plain adapter; the slice rank for a per-slice adapter of a fused linear).
 __global__ void set_slot_kernel(float* slot_scale, int32_t* slot_rank, int slot, float alpha, int rank,
-                                int rslora) {
+                                int scale_rank, int rslora) {
   // c = alpha / r, or alpha / sqrt(r) for rsLoRA ("[vLLM] LoRA", PEFTHelper), fp32, IEEE rounding.
-  const float r = static_cast<float>(rank);
+  const float r = static_cast<float>(scale_rank);
   slot_scale[slot] = rank > 0 ? __fdiv_rn(alpha, rslora ? __fsqrt_rn(r) : r) : 0.0f;
   slot_rank[slot] = rank;
 }
@@ -313,8 +315,13 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
   return MLORA_OK;
 }
 
-static mlora_status write_slot(mlora_pool_t p, int slot, const mlora_bf16* A_host, const mlora_bf16* B_host,
-                               int rank, float alpha, int rslora) {
+// Writes a slot on the pool's copy stream after every call already queued on the pool: zeroes
+// it, then copies n_slices adapters of rank r each; slice i's A [r, K] goes to rows i r .. and its
+// B [widths[i], r] to rows off_i .. (off_i = sum of the earlier widths) and columns i r .. of the
+// slot's B (block-diagonal; a plain adapter is one slice of width D). n_slices = 0 clears it.
+static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, const int* widths,
+                                      const mlora_bf16* const* A_host, const mlora_bf16* const* B_host, int r,
+                                      float alpha, int rslora) {
   cudaStream_t cs = p->copy_stream;
   for (auto& u : p->users) {                   // after every call already queued on the pool
     MLORA_CUDA(cudaEventRecord(p->use_done, u.first), "record use event");
@@ -324,15 +331,21 @@ static mlora_status write_slot(mlora_pool_t p, int slot, const mlora_bf16* A_hos
   uint16_t* b_slot = p->B + static_cast<size_t>(slot) * p->D * p->R;
   MLORA_CUDA(cudaMemsetAsync(a_slot, 0, static_cast<size_t>(p->R) * p->K * 2, cs), "zero slot A");
   MLORA_CUDA(cudaMemsetAsync(b_slot, 0, static_cast<size_t>(p->D) * p->R * 2, cs), "zero slot B");
-  if (rank > 0) {
-    MLORA_CUDA(cudaMemcpyAsync(a_slot, A_host, static_cast<size_t>(rank) * p->K * 2, cudaMemcpyHostToDevice, cs),
+  int off = 0;
+  for (int i = 0; i < n_slices; ++i) {
+    const int w = widths ? widths[i] : p->D;
+    MLORA_CUDA(cudaMemcpyAsync(a_slot + static_cast<size_t>(i) * r * p->K, A_host[i], static_cast<size_t>(r) * p->K * 2,
+                               cudaMemcpyHostToDevice, cs),
                "copy A into slot");
-    MLORA_CUDA(cudaMemcpy2DAsync(b_slot, static_cast<size_t>(p->R) * 2, B_host, static_cast<size_t>(rank) * 2,
-                                 static_cast<size_t>(rank) * 2, static_cast<size_t>(p->D), cudaMemcpyHostToDevice, cs),
+    MLORA_CUDA(cudaMemcpy2DAsync(b_slot + static_cast<size_t>(off) * p->R + static_cast<size_t>(i) * r,
+                                 static_cast<size_t>(p->R) * 2, B_host[i], static_cast<size_t>(r) * 2,
+                                 static_cast<size_t>(r) * 2, static_cast<size_t>(w), cudaMemcpyHostToDevice, cs),
                "copy B into slot");
+    off += w;
   }
+  const int rank = n_slices * r;
   note_launch_begin(kKindSlot, cs);
-  set_slot_kernel<<<1, 1, 0, cs>>>(p->slot_scale, p->slot_rank, slot, alpha, rank, rslora);
+  set_slot_kernel<<<1, 1, 0, cs>>>(p->slot_scale, p->slot_rank, slot, alpha, rank, r, rslora);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindSlot, cs);
   if (e != cudaSuccess) return cuda_fail(e, "set_slot_kernel");
@@ -356,14 +369,41 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const mlora_bf16* A_ho
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev != p->device) return fail(MLORA_ERR_MISMATCH, "pool lives on device %d, current is %d", p->device, dev);
-  return write_slot(p, slot, A_host, B_host, rank, alpha, rslora);
+  return write_slot_sliced(p, slot, 1, nullptr, &A_host, &B_host, rank, alpha, rslora);
+}
+
+mlora_status mlora_load_adapter_sliced(mlora_pool_t p, int slot, int n_slices, const int* widths,
+                                       const mlora_bf16* const* A_slices, const mlora_bf16* const* B_slices, int rank,
+                                       float alpha, int rslora) {
+  if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+  if (slot < 0 || slot >= p->S) return fail(MLORA_ERR_SLOT_RANGE, "slot %d outside [0, %d)", slot, p->S);
+  if (n_slices < 1 || n_slices > MLORA_MAX_SLICES)
+    return fail(MLORA_ERR_INVALID_ARG, "n_slices %d outside [1, %d]", n_slices, MLORA_MAX_SLICES);
+  if (!widths || !A_slices || !B_slices) return fail(MLORA_ERR_INVALID_ARG, "widths or slice arrays are NULL");
+  long total = 0;
+  for (int i = 0; i < n_slices; ++i) {
+    if (widths[i] < 1) return fail(MLORA_ERR_INVALID_ARG, "slice %d has width %d", i, widths[i]);
+    if (!A_slices[i] || !B_slices[i]) return fail(MLORA_ERR_INVALID_ARG, "slice %d: A or B is NULL", i);
+    total += widths[i];
+  }
+  if (total != p->D) return fail(MLORA_ERR_INVALID_ARG, "slice widths add up to %ld, the pool's D is %d", total, p->D);
+  if (rank < 1 || !std::isfinite(alpha))
+    return fail(MLORA_ERR_RANK_INVALID, "rank %d must be >= 1 and alpha finite", rank);
+  if (static_cast<long>(n_slices) * rank > p->r_max)
+    return fail(MLORA_ERR_RANK_TOO_LARGE, "%d slices of rank %d need rank %d, larger than the pool's max rank %d",
+                n_slices, rank, n_slices * rank, p->r_max);
+  std::lock_guard<std::mutex> lk(p->mu);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != p->device) return fail(MLORA_ERR_MISMATCH, "pool lives on device %d, current is %d", p->device, dev);
+  return write_slot_sliced(p, slot, n_slices, widths, A_slices, B_slices, rank, alpha, rslora);
 }
 
 mlora_status mlora_clear_slot(mlora_pool_t p, int slot) {
   if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
   if (slot < 0 || slot >= p->S) return fail(MLORA_ERR_SLOT_RANGE, "slot %d outside [0, %d)", slot, p->S);
   std::lock_guard<std::mutex> lk(p->mu);
-  return write_slot(p, slot, nullptr, nullptr, 0, 0.f, 0);
+  return write_slot_sliced(p, slot, 0, nullptr, nullptr, nullptr, 0, 0.f, 0);
 }
 
 mlora_status mlora_pool_sync(mlora_pool_t p) {

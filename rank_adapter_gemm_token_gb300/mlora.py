@@ -35,6 +35,7 @@ EXPORTS = (
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
     "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n", "mlora_check_wait_timeout",
+    "mlora_load_adapter_sliced",
 )
 
 
@@ -85,6 +86,7 @@ def load(path: str | None = None):
             "mlora_lora_apply_noalloc": [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp],
             "mlora_set_gemm_tile_n": [i32],
             "mlora_check_wait_timeout": [vp],
+            "mlora_load_adapter_sliced": [vp, i32, i32, vp, vp, vp, i32, f32, i32],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -144,6 +146,19 @@ def mlora_load_adapter(pool: int, slot: int, A_host, B_host, rank: int, alpha: f
     """A_host [rank, K] and B_host [D, rank]: host bf16 (uint16 numpy arrays or CPU torch tensors)."""
     a, b = _host_ptr(A_host), _host_ptr(B_host)
     _check(load().mlora_load_adapter(pool, slot, a, b, rank, float(alpha), int(bool(rslora))), "mlora_load_adapter")
+
+
+def mlora_load_adapter_sliced(pool: int, slot: int, A_slices, B_slices, rank: int, alpha: float,
+                              rslora: bool) -> None:
+    """Per-slice adapter of a fused linear: A_slices[i] [rank, K], B_slices[i] [width_i, rank] host
+    bf16 (uint16 numpy arrays or CPU torch tensors); the widths are the B slices' row counts."""
+    n = len(A_slices)
+    assert len(B_slices) == n
+    widths = (ctypes.c_int * n)(*[int(b.shape[0]) for b in B_slices])
+    a_ptrs = (ctypes.c_void_p * n)(*[_host_ptr(a) for a in A_slices])
+    b_ptrs = (ctypes.c_void_p * n)(*[_host_ptr(b) for b in B_slices])
+    _check(load().mlora_load_adapter_sliced(pool, slot, n, widths, a_ptrs, b_ptrs, rank, float(alpha),
+                                            int(bool(rslora))), "mlora_load_adapter_sliced")
 
 
 def mlora_clear_slot(pool: int, slot: int) -> None:

@@ -300,3 +300,57 @@ def test_overflow_window(cuda_device, J, seed, T, ovf):
     dw.meta.status()
     _check_linear(wl, dw, dw.linears[0])
     dw.close()
+
+
+@pytest.mark.parametrize("T,J,r,r_max,seed", [(100, 1, 8, 32, 60), (100, 2, 8, 32, 61), (700, 1, 16, 64, 62)])
+def test_sliced_adapters_of_a_fused_linear(cuda_device, T, J, r, r_max, seed):
+    """Per-slice adapters of a fused qkv-like linear (slices 256 / 64 / 64 wide), loaded with
+    mlora_load_adapter_sliced, against the oracle that computes each slice as its own linear.
+    T = 100 takes the small-batch path, T = 700 (runs of one slot, rank width 64) the tensor-core
+    prefill path."""
+    import torch
+    from types import SimpleNamespace
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    rng = np.random.default_rng(seed)
+    K, widths, S = 512, [256, 64, 64], 6
+    D = sum(widths)
+    W = synth.normal_bf16(seed, 10, (D, K), 0.02)
+    x = synth.normal_bf16(seed, 11, (T, K), 1.0)
+    sliced = {}
+    for s in range(S):
+        alpha, rs = float(2 * r), bool(s % 2)
+        sliced[s] = [SimpleNamespace(A=synth.normal_bf16(seed, 100 + 10 * s + i, (r, K), 0.02),
+                                     B=synth.normal_bf16(seed, 500 + 10 * s + i, (w, r), 0.02),
+                                     rank=r, alpha=alpha, rslora=rs) for i, w in enumerate(widths)]
+    if T > 256:
+        slots = np.repeat(rng.integers(-1, S, size=(T + 127) // 128), 128)[:T].reshape(T, 1).astype(np.int32)
+        slots = np.concatenate([slots] * J, axis=1)
+    else:
+        slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    pool = layer.AdapterPool(S, r_max, K, D)
+    for s, parts in sliced.items():
+        mlora.mlora_load_adapter_sliced(pool.handle, s, [p.A for p in parts], [p.B for p in parts], r,
+                                        parts[0].alpha, parts[0].rslora)
+    pool.sync()
+    meta = layer.StepMeta(T, J, r_max)
+    meta.build(torch.from_numpy(slots).cuda(), torch.from_numpy(scales).cuda(), pool)
+    y = layer.linear(pool, meta, layer.bf16_from_bits(x, "cuda"), layer.bf16_from_bits(W, "cuda"))
+    meta.status()
+    ref = oracle.linear_sliced(x, W, slots, sliced, S, widths, scales=scales)
+    assert_close(y.cpu().numpy(), ref, f"sliced T={T} J={J}")
+    meta.close()
+    pool.close()
+
+
+def test_sliced_adapter_argument_checks(cuda_device):
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    pool = layer.AdapterPool(2, 16, 64, 48)
+    A = np.zeros((8, 64), np.uint16)
+    with pytest.raises(mlora.MloraError) as e:           # widths must add up to D
+        mlora.mlora_load_adapter_sliced(pool.handle, 0, [A, A], [np.zeros((20, 8), np.uint16)] * 2, 8, 16.0, False)
+    assert e.value.status == mlora.MLORA_ERR_INVALID_ARG
+    with pytest.raises(mlora.MloraError) as e:           # 3 slices x rank 8 > r_max 16
+        mlora.mlora_load_adapter_sliced(pool.handle, 0, [A] * 3, [np.zeros((16, 8), np.uint16)] * 3, 8, 16.0, False)
+    assert e.value.status == mlora.MLORA_ERR_RANK_TOO_LARGE
+    pool.close()

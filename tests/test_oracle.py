@@ -120,6 +120,50 @@ def test_two_adapters_equal_their_cat_merge(seed):
     assert np.max(np.abs(y - y_cat)) <= 1e-12 * np.max(np.abs(y_cat))
 
 
+@pytest.mark.parametrize("rslora", [False, True])
+def test_sliced_adapter_equals_its_block_diagonal_form(rslora):
+    # A fused linear with one adapter per output slice equals one adapter of rank n r with
+    # A = [A_1; ...; A_n] and block-diagonal B (slice i's rows hold B_i in columns i r ..), whose
+    # factor is that of the slices (alpha scaled so that alpha' / (n r) or alpha' / sqrt(n r)
+    # equals alpha / r or alpha / sqrt(r)). Also: each slice's outputs differ from the base only
+    # through that slice's own adapter.
+    rng = np.random.default_rng(31)
+    T, K, J, S, r = 6, 20, 2, 3, 3
+    widths = [7, 4, 5]
+    D = sum(widths)
+    x, W = rng.standard_normal((T, K)), rng.standard_normal((D, K))
+    sliced = {}
+    for s in range(S):
+        alpha = float(rng.integers(1, 9))
+        sliced[s] = [SimpleNamespace(A=rng.standard_normal((r, K)), B=rng.standard_normal((w, r)), rank=r,
+                                     alpha=alpha, rslora=rslora) for w in widths]
+    slots = rng.integers(-1, S, size=(T, J))
+    scales = rng.uniform(0.2, 1.0, size=(T, J))
+    y = oracle.linear_sliced(x, W, slots, sliced, S, widths, scales=scales)
+    n = len(widths)
+    whole = {}
+    for s, parts in sliced.items():
+        B = np.zeros((D, n * r))
+        off = 0
+        for i, (w, p) in enumerate(zip(widths, parts)):
+            B[off:off + w, i * r:(i + 1) * r] = p.B
+            off += w
+        a0 = parts[0].alpha
+        whole[s] = SimpleNamespace(A=np.vstack([p.A for p in parts]), B=B, rank=n * r,
+                                   alpha=a0 * (np.sqrt(n) if rslora else n), rslora=rslora)
+    y_whole = oracle.linear(x, W, slots, whole, S, scales=scales)
+    assert np.max(np.abs(y - y_whole)) <= 1e-12 * np.max(np.abs(y_whole))
+    # slice 1 alone: its adapter, written out
+    t, (s0, s1) = 2, slots[2]
+    lo, hi = widths[0], widths[0] + widths[1]
+    ref = W[lo:hi] @ x[t]
+    for j, s in enumerate((s0, s1)):
+        if s >= 0:
+            p = sliced[s][1]
+            ref = ref + scales[t, j] * _factor(p) * (p.B @ (p.A @ x[t]))
+    assert np.max(np.abs(y[t, lo:hi] - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
 def test_output_is_linear_in_the_scale():
     c = _random_case(7, J=1)
     slots = np.full((c["T"], 1), 2)
