@@ -50,6 +50,8 @@ typedef int mlora_status;
 typedef uint16_t mlora_bf16;
 typedef struct mlora_pool* mlora_pool_t;
 typedef struct mlora_meta* mlora_meta_t;
+typedef struct mlora_slot_cache* mlora_slot_cache_t;
+typedef struct mlora_adapter_cache* mlora_adapter_cache_t;
 
 enum {
   MLORA_OK = 0,
@@ -62,7 +64,8 @@ enum {
   MLORA_ERR_OOM = 7,              /* device or host allocation failed                       */
   MLORA_ERR_CUDA = 8,             /* a CUDA call failed (message has the CUDA error)         */
   MLORA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait gave up (the GPU stays usable)  */
-  MLORA_ERR_MISMATCH = 10         /* pool and metadata or pool and operands do not fit     */
+  MLORA_ERR_MISMATCH = 10,        /* pool and metadata or pool and operands do not fit     */
+  MLORA_ERR_NO_FREE_SLOT = 11     /* a step needs more adapters resident than slots allow  */
 };
 
 /* Limits of this build. */
@@ -220,6 +223,48 @@ MLORA_API mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, c
                                                 const mlora_bf16* B_pool, const float* slot_scale,
                                                 const int32_t* slot_rank, int n_slots, int r_pad, int K, int D,
                                                 void* stream);
+
+/* ------------------------------------------------------------------ slot residency ---- */
+
+/* Which adapter id sits in which of n_slots GPU slots ("LoRA Serving", section 5: the LRU cache
+ * model manager marks a hit as recent and on a miss evicts the oldest adapter that is not pinned;
+ * "Multi-LoRA Serving Explained", serving section: a fixed number of GPU slots, least recently
+ * used pushed out). Host logic only, no GPU work.
+ * mlora_slot_cache_assign maps the ids of one step (n entries, e.g. one per token and slot;
+ * -1 = no adapter -> slot -1) to slots: a resident id keeps its slot; each other id takes the
+ * lowest free slot, else the slot used longest ago (lowest index on ties) that no id of this step
+ * and no pinned id holds. Writes slots[n] and the (id, slot) pairs that must be loaded (first-seen
+ * order) to load_ids / load_slots (capacity n each; either may be NULL) and their count to
+ * *n_loads. MLORA_ERR_NO_FREE_SLOT when the step names more distinct ids than free or evictable
+ * slots allow; nothing changes then. lookup gives an id's slot (-1 if not resident); pin keeps a
+ * resident id from eviction (pinned != 0) or releases it; evict frees an id's slot. */
+MLORA_API mlora_status mlora_slot_cache_create(int n_slots, mlora_slot_cache_t* out);
+MLORA_API mlora_status mlora_slot_cache_destroy(mlora_slot_cache_t cache);
+MLORA_API mlora_status mlora_slot_cache_assign(mlora_slot_cache_t cache, const int64_t* ids, int n, int32_t* slots,
+                                               int64_t* load_ids, int32_t* load_slots, int* n_loads);
+MLORA_API mlora_status mlora_slot_cache_lookup(mlora_slot_cache_t cache, int64_t id, int32_t* slot);
+MLORA_API mlora_status mlora_slot_cache_pin(mlora_slot_cache_t cache, int64_t id, int pinned);
+MLORA_API mlora_status mlora_slot_cache_evict(mlora_slot_cache_t cache, int64_t id);
+
+/* The slot cache over the pools of one model (one pool per adapted linear, all with the same
+ * n_slots): adapters registered by id with one host (A, B) pair per pool, in pool order
+ * (A_host[i] [rank, K_i], B_host[i] [D_i, rank], bf16; the caller keeps them valid while
+ * registered, pinned for asynchronous loads). mlora_adapter_cache_map assigns the step's ids as
+ * mlora_slot_cache_assign does, queues mlora_load_adapter into every pool for each id that is
+ * not resident (asynchronous on the pools' copy streams; each pool's next mlora_linear orders
+ * itself after them) and writes the host token -> slot map token_slots[n] for mlora_build_meta.
+ * An unregistered id: MLORA_ERR_INVALID_ARG, nothing changes. Registering an id again replaces
+ * its buffers and drops its resident copy (the next step loads the new one); unregister also
+ * unpins it. */
+MLORA_API mlora_status mlora_adapter_cache_create(const mlora_pool_t* pools, int n_pools, mlora_adapter_cache_t* out);
+MLORA_API mlora_status mlora_adapter_cache_destroy(mlora_adapter_cache_t cache);
+MLORA_API mlora_status mlora_adapter_cache_register(mlora_adapter_cache_t cache, int64_t id,
+                                                    const mlora_bf16* const* A_host, const mlora_bf16* const* B_host,
+                                                    int rank, float alpha, int rslora);
+MLORA_API mlora_status mlora_adapter_cache_unregister(mlora_adapter_cache_t cache, int64_t id);
+MLORA_API mlora_status mlora_adapter_cache_pin(mlora_adapter_cache_t cache, int64_t id, int pinned);
+MLORA_API mlora_status mlora_adapter_cache_map(mlora_adapter_cache_t cache, const int64_t* ids, int n,
+                                               int32_t* token_slots, int* n_loaded);
 
 /* ------------------------------------------------------------------ diagnostics ------ */
 

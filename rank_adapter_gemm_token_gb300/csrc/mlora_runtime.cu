@@ -224,6 +224,7 @@ const char* mlora_status_string(mlora_status s) {
     case MLORA_ERR_CUDA: return "CUDA error";
     case MLORA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
     case MLORA_ERR_MISMATCH: return "pool, metadata and operands do not fit together";
+    case MLORA_ERR_NO_FREE_SLOT: return "more adapters needed at once than free or evictable slots";
     default: return "unknown status";
   }
 }

@@ -25,6 +25,7 @@ MLORA_ERR_OOM = 7
 MLORA_ERR_CUDA = 8
 MLORA_ERR_DEVICE_TIMEOUT = 9
 MLORA_ERR_MISMATCH = 10
+MLORA_ERR_NO_FREE_SLOT = 11
 
 KERNEL_KINDS = ("meta", "base_gemm", "shrink", "expand", "slot")
 
@@ -35,7 +36,10 @@ EXPORTS = (
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
     "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n", "mlora_check_wait_timeout",
-    "mlora_load_adapter_sliced",
+    "mlora_load_adapter_sliced", "mlora_slot_cache_create", "mlora_slot_cache_destroy", "mlora_slot_cache_assign",
+    "mlora_slot_cache_lookup", "mlora_slot_cache_pin", "mlora_slot_cache_evict", "mlora_adapter_cache_create",
+    "mlora_adapter_cache_destroy", "mlora_adapter_cache_register", "mlora_adapter_cache_unregister",
+    "mlora_adapter_cache_pin", "mlora_adapter_cache_map",
 )
 
 
@@ -87,6 +91,18 @@ def load(path: str | None = None):
             "mlora_set_gemm_tile_n": [i32],
             "mlora_check_wait_timeout": [vp],
             "mlora_load_adapter_sliced": [vp, i32, i32, vp, vp, vp, i32, f32, i32],
+            "mlora_slot_cache_create": [i32, vp],
+            "mlora_slot_cache_destroy": [vp],
+            "mlora_slot_cache_assign": [vp, vp, i32, vp, vp, vp, vp],
+            "mlora_slot_cache_lookup": [vp, ctypes.c_int64, vp],
+            "mlora_slot_cache_pin": [vp, ctypes.c_int64, i32],
+            "mlora_slot_cache_evict": [vp, ctypes.c_int64],
+            "mlora_adapter_cache_create": [vp, i32, vp],
+            "mlora_adapter_cache_destroy": [vp],
+            "mlora_adapter_cache_register": [vp, ctypes.c_int64, vp, vp, i32, f32, i32],
+            "mlora_adapter_cache_unregister": [vp, ctypes.c_int64],
+            "mlora_adapter_cache_pin": [vp, ctypes.c_int64, i32],
+            "mlora_adapter_cache_map": [vp, vp, i32, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -247,6 +263,85 @@ def mlora_lora_apply_noalloc(x, y, token_slots, scales, T: int, J: int, A_pool, 
 def mlora_set_gemm_tile_n(n: int) -> None:
     """0 automatic, -1 never the CTA-pair GEMM, 256/224/192/128 always it with that N tile."""
     _check(load().mlora_set_gemm_tile_n(n), "mlora_set_gemm_tile_n")
+
+
+# ------------------------------------------------------------------------- slot residency
+def mlora_slot_cache_create(n_slots: int) -> int:
+    out = ctypes.c_void_p()
+    _check(load().mlora_slot_cache_create(n_slots, ctypes.byref(out)), "mlora_slot_cache_create")
+    return out.value
+
+
+def mlora_slot_cache_destroy(cache: int) -> None:
+    _check(load().mlora_slot_cache_destroy(cache), "mlora_slot_cache_destroy")
+
+
+def mlora_slot_cache_assign(cache: int, ids) -> tuple:
+    """(slots [n] int32, loads [(id, slot), ...]) for one step's adapter ids (-1 = none)."""
+    import numpy as np
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int64).ravel())
+    n = len(ids)
+    slots = np.zeros(max(n, 1), np.int32)
+    load_ids = np.zeros(max(n, 1), np.int64)
+    load_slots = np.zeros(max(n, 1), np.int32)
+    n_loads = ctypes.c_int()
+    _check(load().mlora_slot_cache_assign(cache, ids.ctypes.data, n, slots.ctypes.data, load_ids.ctypes.data,
+                                          load_slots.ctypes.data, ctypes.byref(n_loads)), "mlora_slot_cache_assign")
+    k = n_loads.value
+    return slots[:n], list(zip(load_ids[:k].tolist(), load_slots[:k].tolist()))
+
+
+def mlora_slot_cache_lookup(cache: int, adapter_id: int) -> int:
+    out = ctypes.c_int32()
+    _check(load().mlora_slot_cache_lookup(cache, adapter_id, ctypes.byref(out)), "mlora_slot_cache_lookup")
+    return out.value
+
+
+def mlora_slot_cache_pin(cache: int, adapter_id: int, pinned: bool = True) -> None:
+    _check(load().mlora_slot_cache_pin(cache, adapter_id, int(bool(pinned))), "mlora_slot_cache_pin")
+
+
+def mlora_slot_cache_evict(cache: int, adapter_id: int) -> None:
+    _check(load().mlora_slot_cache_evict(cache, adapter_id), "mlora_slot_cache_evict")
+
+
+def mlora_adapter_cache_create(pools) -> int:
+    arr = (ctypes.c_void_p * len(pools))(*pools)
+    out = ctypes.c_void_p()
+    _check(load().mlora_adapter_cache_create(arr, len(pools), ctypes.byref(out)), "mlora_adapter_cache_create")
+    return out.value
+
+
+def mlora_adapter_cache_destroy(cache: int) -> None:
+    _check(load().mlora_adapter_cache_destroy(cache), "mlora_adapter_cache_destroy")
+
+
+def mlora_adapter_cache_register(cache: int, adapter_id: int, A_host, B_host, rank: int, alpha: float,
+                                 rslora: bool) -> None:
+    """A_host / B_host: one host bf16 buffer per pool (kept alive by the caller while registered)."""
+    a = (ctypes.c_void_p * len(A_host))(*[_host_ptr(x) for x in A_host])
+    b = (ctypes.c_void_p * len(B_host))(*[_host_ptr(x) for x in B_host])
+    _check(load().mlora_adapter_cache_register(cache, adapter_id, a, b, rank, float(alpha), int(bool(rslora))),
+           "mlora_adapter_cache_register")
+
+
+def mlora_adapter_cache_unregister(cache: int, adapter_id: int) -> None:
+    _check(load().mlora_adapter_cache_unregister(cache, adapter_id), "mlora_adapter_cache_unregister")
+
+
+def mlora_adapter_cache_pin(cache: int, adapter_id: int, pinned: bool = True) -> None:
+    _check(load().mlora_adapter_cache_pin(cache, adapter_id, int(bool(pinned))), "mlora_adapter_cache_pin")
+
+
+def mlora_adapter_cache_map(cache: int, ids) -> tuple:
+    """(token_slots [n] int32 host array, number of adapters loaded) for one step's adapter ids."""
+    import numpy as np
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int64).ravel())
+    slots = np.zeros(max(len(ids), 1), np.int32)
+    n_loaded = ctypes.c_int()
+    _check(load().mlora_adapter_cache_map(cache, ids.ctypes.data, len(ids), slots.ctypes.data,
+                                          ctypes.byref(n_loaded)), "mlora_adapter_cache_map")
+    return slots[:len(ids)], n_loaded.value
 
 
 # ------------------------------------------------------------------------- diagnostics
