@@ -499,6 +499,12 @@ def run_ours(args):
             entry["achieved_TFLOPs"] = algo["base_flops"] / per / (t / n / 1000.0) / 1e12
             entry["frac_bf16"] = entry["achieved_TFLOPs"] / peaks["bf16_tflops"]
         per_kernel[k] = entry
+    # the whole step against its own bound: the slower of (all algorithmic bytes / HBM peak) and
+    # (all flops / bf16 peak), over the measured step time
+    step_bytes = sum(v for k, v in algo.items() if k not in ("base_flops",))
+    bound_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), algo["base_flops"] / (peaks["bf16_tflops"] * 1e12))
+    step_roofline = {"bound_us": bound_s * 1e6, "frac": bound_s / (ms / 1000.0),
+                     "bytes_per_step": step_bytes, "flops_per_step": algo["base_flops"]}
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
@@ -517,6 +523,7 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clock_info,
         "kernels": per_kernel,
+        "step_roofline": step_roofline,
         "wall_s_timed_region": wall,
         "kernel_timing": f"second pass of {trace_steps} steps with per-kernel CUDA events on the launch stream",
         "step_launch": "CUDA graph replay of the captured step" if graph is not None else "direct calls",
