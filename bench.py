@@ -437,19 +437,58 @@ def run_ours(args):
     h2d = sum(v.numel() * v.element_size() for v in xs_host.values()) + slots_host.numel() * 4 + \
         (0 if scales_host is None else scales_host.numel() * 4)
     d2h = sum(y.numel() * y.element_size() for y in ys_host)
+    # The step as a user would pipeline it through the public API: the inputs go up on a copy
+    # stream, each linear waits only for its own input, and each output goes down on a second
+    # copy stream while the next linear computes. Captured once as a graph (with the flag
+    # --no-graph, issued directly each step).
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def e2e_step(s):
+        up.wait_stream(s)
+        down.wait_stream(s)
+        ev_x = {}
+        with torch.cuda.stream(up):
+            dw.token_slots.copy_(slots_host, non_blocking=True)
+            if scales_host is not None:
+                dw.scales.copy_(scales_host, non_blocking=True)
+            ev_meta = torch.cuda.Event()
+            ev_meta.record(up)
+            for k, v in xs_host.items():
+                dw.x[k].copy_(v, non_blocking=True)
+                ev_x[k] = torch.cuda.Event()
+                ev_x[k].record(up)
+        s.wait_event(ev_meta)
+        dw.build_meta(s)
+        for dl, yh in zip(dw.linears, ys_host):
+            s.wait_event(ev_x[dl.lin.x_id])
+            dw.layer.linear(dl.pool, dw.meta, dw.x[dl.lin.x_id], dl.W, dl.y, s)
+            ev_y = torch.cuda.Event()
+            ev_y.record(s)
+            down.wait_event(ev_y)
+            with torch.cuda.stream(down):
+                yh.copy_(dl.y, non_blocking=True)
+        s.wait_stream(up)
+        s.wait_stream(down)
+
+    e2e_run = lambda: e2e_step(stream)  # noqa: E731
+    if not args.no_graph:
+        cap = torch.cuda.Stream(device)
+        e2e_step(cap)                    # first use of the streams and events, outside the capture
+        torch.cuda.synchronize(device)
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph, stream=cap):
+            e2e_step(cap)
+        torch.cuda.synchronize(device)
+        e2e_run = e2e_graph.replay
+    for _ in range(args.warmup):
+        e2e_run()
+    torch.cuda.synchronize(device)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(args.steps):
         flush.zero_()
         e_start.record(stream)
-        for k, v in xs_host.items():
-            dw.x[k].copy_(v, non_blocking=True)
-        dw.token_slots.copy_(slots_host, non_blocking=True)
-        if scales_host is not None:
-            dw.scales.copy_(scales_host, non_blocking=True)
-        run_step()
-        for dl, yh in zip(dw.linears, ys_host):
-            yh.copy_(dl.y, non_blocking=True)
+        e2e_run()
         e_end.record(stream)
         e_end.synchronize()
         e2e_ms.append(e_start.elapsed_time(e_end))
