@@ -354,3 +354,34 @@ def test_sliced_adapter_argument_checks(cuda_device):
         mlora.mlora_load_adapter_sliced(pool.handle, 0, [A] * 3, [np.zeros((16, 8), np.uint16)] * 3, 8, 16.0, False)
     assert e.value.status == mlora.MLORA_ERR_RANK_TOO_LARGE
     pool.close()
+
+
+@pytest.mark.parametrize("T,J,R,seed", [(90, 1, 16, 70), (90, 2, 24, 71), (600, 1, 64, 72), (600, 3, 16, 73)])
+def test_separate_gemm_shrink_expand_entry_points(cuda_device, T, J, R, seed):
+    """mlora_base_gemm, then mlora_lora_shrink and mlora_lora_expand (the CUDA-core kernels, one
+    call each) give the layer's output."""
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    rng = np.random.default_rng(seed)
+    K, D, S = 264, 200, 9
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = int(rng.integers(1, R + 1))
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(seed, 300 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(2 * r), rslora=bool(s % 2))
+    slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("separate", seed, T, J, S, R, slots, scales, {0: synth.normal_bf16(seed, 11, (T, K), 1.0)},
+                        [lin])
+    dw = DeviceWorkload(wl)
+    dw.build_meta()
+    dl = dw.linears[0]
+    x = dw.x[0]
+    y = layer.base_gemm(x, dl.W)
+    mlora.mlora_lora_shrink(dl.pool.handle, dw.meta.handle, x)
+    mlora.mlora_lora_expand(dl.pool.handle, dw.meta.handle, y)
+    torch.cuda.synchronize()
+    dw.meta.status()
+    assert_close(y.cpu().numpy(), oracle_rows(wl, lin), "separate entry points")
+    dw.close()
