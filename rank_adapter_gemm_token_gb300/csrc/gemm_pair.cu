@@ -346,14 +346,16 @@ cudaError_t launch_pair_bn(const uint16_t* x, const uint16_t* W, float* y, int T
   return e;
 }
 
-// Fraction of the pairs' tile time that does useful work for N tile bn: columns computed that
-// are real (D over whole tiles) times busy pairs over the waves (the last wave may be partial).
-double pair_efficiency(int T, int D, int bn, int max_pairs) {
+// Estimated launch time for N tile bn, in units of one 256 x 256 pair tile: whole waves of the
+// resident pairs (a partial last wave costs a full one) times the time of one tile. That time is
+// mostly independent of the tile's width (x staging, pipeline fill, epilogue) and only partly
+// proportional to it; the split is fitted to single-launch timings of the four widths at
+// T = 512-2048, K = 4096-14336 on GB300.
+double pair_time(int T, int D, int bn, int max_pairs) {
   const long mp = ((T + kHalf - 1) / kHalf + 1) / 2;
-  const long nb = (D + bn - 1) / bn;
-  const long tiles = mp * nb;
+  const long tiles = mp * ((D + bn - 1) / bn);
   const long waves = (tiles + max_pairs - 1) / max_pairs;
-  return (static_cast<double>(D) / (nb * bn)) * (static_cast<double>(tiles) / (waves * max_pairs));
+  return static_cast<double>(waves) * (0.83 + 0.17 * bn / 256.0);
 }
 
 }  // namespace
@@ -394,12 +396,11 @@ int pair_gemm_max_pairs() {
 int pair_gemm_pick_n(int T, int D, int max_pairs) {
   static const int kChoices[] = {256, 224, 192, 128};
   int best = 256;
-  double best_eff = -1.0;
-  for (int bn : kChoices) {
-    // narrower tiles stage more W per flop: ask for a clear gain before taking one
-    const double eff = pair_efficiency(T, D, bn, max_pairs) * (1.0 - 0.1 * (256 - bn) / 128.0);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+  double best_time = 0.0;
+  for (int bn : kChoices) {                    // the widest of equally fast choices
+    const double t = pair_time(T, D, bn, max_pairs);
+    if (bn == 256 || t < best_time - 1e-9) {
+      best_time = t;
       best = bn;
     }
   }

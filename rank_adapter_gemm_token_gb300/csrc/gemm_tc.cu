@@ -663,13 +663,15 @@ cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y
     SkinnyShrink none{};
     return launch_skinny(x, W, y, T, K, D, err, num_sms, nullptr, 0, none, s);
   }
-  // Enough 256 x 256 tiles for every CTA pair: the pair kernel. Otherwise the largest one-CTA
-  // N tile that still gives every SM a tile; small problems take N = 64.
+  // Two or more 128-row tiles: the CTA-pair kernel whenever it is available, its N tile chosen by
+  // estimated time. Even a single partial wave of 256-row pair tiles beats the one-CTA kernel's
+  // narrower tiles on every shape measured (T = 512-2048). One 128-row tile, or
+  // mlora_set_gemm_tile_n(-1): the one-CTA kernel with the largest N tile that still gives every
+  // SM a tile; small problems take N = 64.
   const int m_tiles = (T + BM - 1) / BM;
   const int forced_n = gemm_tile_n();
   if (forced_n > 0) return launch_pair_gemm(x, W, y, T, K, D, err, pool, meta, forced_n, s);
-  const int max_pairs = forced_n < 0 ? 0 : pair_gemm_max_pairs();
-  if (max_pairs > 0 && ((m_tiles + 1) / 2) * ((D + 255) / 256) >= max_pairs)
+  if (forced_n == 0 && m_tiles > 1 && pair_gemm_max_pairs() > 0)
     return launch_pair_gemm(x, W, y, T, K, D, err, pool, meta, 0, s);
   if (m_tiles * ((D + 255) / 256) >= num_sms)
     return launch_tc<256, 4>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
