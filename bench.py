@@ -69,6 +69,8 @@ def make_workload(name: str):
     import synth
     if name == "decode":
         return synth.decode()
+    if name == "logits":
+        return synth.logits()
     if name == "compose":
         return synth.compose()
     if name == "tiny":
@@ -96,11 +98,11 @@ def workload_config(wl, name: str) -> dict:
     }
 
 
-def algorithmic_bytes(wl) -> dict:
+def algorithmic_bytes(wl, num_sms: int = 152) -> dict:
     """Bytes each kernel kind must move per step (unique data, each counted once), by path.
 
-    Small batches (T <= 256: one split-K tensor-core kernel computes the base product and the
-    shrink of every active slot): base_gemm = W + x + y write (fp32) + A rows of the active slots
+    Small batches (T <= 256 and every output's 128-column blocks within one wave of the SMs: one
+    split-K tensor-core kernel computes the base product and the shrink of every active slot): base_gemm = W + x + y write (fp32) + A rows of the active slots
     (R rows each, the pool's padded rank) + v write (T x active slots x R, fp32); expand = B rows
     of the active slots at the true rank padded to 8 + read and write of y rows with an active
     slot + v reads of the active pairs.
@@ -114,8 +116,8 @@ def algorithmic_bytes(wl) -> dict:
     slots = wl.token_slots
     active = slots >= 0
     R = (wl.r_max + 7) // 8 * 8
-    small = wl.T <= 256
-    tensor_core = not small and R == 64
+    small = wl.T <= 256 and all((l.D + 127) // 128 <= num_sms for l in wl.linears)
+    tensor_core = wl.T > 256 and R == 64
     fused = np.zeros_like(active)
     tile_slots = []                                   # distinct slots of each fused 128-token tile
     if tensor_core:
@@ -581,7 +583,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny", "mixed"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny", "mixed", "logits"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the library directly for every step")

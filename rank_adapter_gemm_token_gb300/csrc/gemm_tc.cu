@@ -659,7 +659,7 @@ cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y
                                   uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
                                   cudaStream_t s) {
   if (T == 0 || D == 0) return cudaSuccess;
-  if (T <= kSkinnyMaxT && !pool) {
+  if (T <= kSkinnyMaxT && !pool && (D + BM - 1) / BM <= num_sms) {   // its column blocks fill one wave
     SkinnyShrink none{};
     return launch_skinny(x, W, y, T, K, D, err, num_sms, nullptr, 0, none, s);
   }

@@ -675,9 +675,11 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   const MetaView mv = m->view();
   const PoolView pv = p->view();
   cudaError_t e = cudaSuccess;
-  if (skinny_shrink_fusable(m->T, m->J, p->S, p->R, m->vfull_ld)) {
-    // small batch: one split-K tensor-core kernel for the base product and the shrink of every
-    // active slot, then the expand as its programmatic dependent
+  if (skinny_shrink_fusable(m->T, m->J, p->S, p->R, m->vfull_ld) && (p->D + 127) / 128 <= ds->num_sms) {
+    // small batch whose 128-column output blocks fit in one wave: one split-K tensor-core kernel
+    // for the base product and the shrink of every active slot, then the expand as its
+    // programmatic dependent (wider outputs, an LM head for instance, take the tiled GEMM and the
+    // separate shrink and expand below)
     if ((e = launch_gemm_shrink_fused(x, W, y, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "fused GEMM launch");
     if ((e = launch_lora_expand_vfull(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");

@@ -247,6 +247,40 @@ def compose(T: int = 128, hidden: int = 4096, qkv_out: int = 6144, n_adapters: i
     return Workload("compose", seed, T, J, n_adapters, rank, slots, scales, xs, [lin])
 
 
+def logits(T: int = 256, hidden: int = 4096, vocab: int = 128256, n_adapters: int = 16,
+           ranks: tuple = (8, 16, 32), J: int = 2, sentinel_frac: float = 0.1,
+           seed_offset: int = 6) -> Workload:
+    """The side path on the LM head with router-weighted mixtures: T decode tokens through the
+    hidden -> vocab linear (Llama-3-sized vocabulary by default); every token mixes J distinct
+    adapters drawn without replacement from n_adapters, weighted by per-token gate values (a
+    softmax over J router logits drawn N(0, 1), as a learned per-token router would emit);
+    sentinel_frac of the tokens use no adapter. Adapter i has rank ranks[i % len(ranks)] and
+    alpha = 2r; the pool's rank width is max(ranks)."""
+    seed = SEED_BASE + seed_offset
+    words = raw_u64(seed, tensor_key(_NS_SLOTS, 0), T * J).reshape(T, J)
+    none = uniform01(seed, tensor_key(_NS_SLOTS, 1), T) < sentinel_frac
+    slots = np.full((T, J), -1, dtype=np.int32)
+    for t in range(T):
+        if none[t]:
+            continue
+        pool = list(range(n_adapters))
+        for j in range(J):                      # partial Fisher-Yates, without replacement
+            i = j + int(words[t, j] % np.uint64(n_adapters - j))
+            pool[j], pool[i] = pool[i], pool[j]
+            slots[t, j] = pool[j]
+    z = normal_f64(seed, tensor_key(_NS_SCALES, 0), (T, J))
+    g = np.exp(z - z.max(axis=1, keepdims=True))
+    scales = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
+    scales[slots < 0] = 0.0
+    r_max = max(ranks)
+    lin = Linear("lm_head", hidden, vocab, normal_bf16(seed, tensor_key(_NS_W, 0, 0), (vocab, hidden), 0.02), 0)
+    for s in range(n_adapters):
+        r = ranks[s % len(ranks)]
+        lin.adapters[s] = _adapter(seed, 0, 0, s, hidden, vocab, r, 2.0 * r, False)
+    xs = {0: normal_bf16(seed, tensor_key(_NS_X, 0), (T, hidden), 1.0)}
+    return Workload("logits", seed, T, J, n_adapters, r_max, slots, scales, xs, [lin])
+
+
 def zipf_admission(n_requests: int, n_ids: int, exponent: float, max_distinct: int,
                    seed: int, tid: int) -> list:
     """Draw request tenants from Zipf(exponent) over ids 1..n_ids and admit them in order: a

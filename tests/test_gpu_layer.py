@@ -154,6 +154,21 @@ def test_prefill_config_full_size(cuda_device):
     dw.close()
 
 
+@pytest.mark.parametrize("T", [256, 1024])
+def test_lm_head_router_mixture(cuda_device, T):
+    """The side path on the LM head (hidden 4096 -> a 32000-entry vocabulary) with router-weighted
+    mixtures: two adapters per token with per-token gate weights ("[RFC] Per-request activation
+    of multiple LoRA adapters", related work: router-driven mixtures; "[vLLM] LoRA",
+    add_lora_logits: the LM head takes the same shrink and expand). T = 256 takes the
+    small-batch path, T = 1024 the larger-batch path of a 32-wide pool."""
+    wl = synth.logits(T=T, vocab=32000)
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0], rows=sample_rows(wl, 12))
+    dw.close()
+
+
 def test_zero_scale_and_linearity_on_gpu(cuda_device):
     import torch
     wl = synth.compose(T=64)

@@ -61,3 +61,16 @@ def test_recipes_shapes_and_distributions():
 def test_admission_rule_defers_new_adapters():
     adm = synth.zipf_admission(300, 1000, 1.1, 5, 123, 9)
     assert len(set(adm)) <= 5 and len(adm) == 300
+
+
+def test_lm_head_mixture_recipe():
+    w = synth.logits(T=200, vocab=512, hidden=256)
+    slots, g = w.token_slots, w.scales
+    idle = np.all(slots < 0, axis=1)
+    assert 0.03 < idle.mean() < 0.2                                       # about 10 % without adapters
+    act = ~idle
+    assert np.all(slots[act] >= 0) and all(len(set(r)) == w.J for r in slots[act].tolist())
+    assert np.allclose(g[act].sum(axis=1), 1.0, atol=1e-6) and np.all(g[act] > 0)   # gate weights
+    assert np.all(g[idle] == 0)
+    assert {a.rank for a in w.linears[0].adapters.values()} == {8, 16, 32} and w.r_max == 32
+    assert w.linears[0].W.shape == (512, 256)
