@@ -313,9 +313,11 @@ def run_reference(args):
 # Sources each recorded kernel is built from; a traffic record holds only while they are unchanged.
 KERNEL_SOURCES = {
     ("decode", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
-    ("decode", "expand"): ("lora_kernels.cu", "expand_vfull.cuh", "ptx.cuh", "internal.h"),
+    ("decode", "expand"): ("expand_vfull.cu", "expand_vfull.cuh", "ptx.cuh", "internal.h"),
     ("prefill", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
     ("prefill", "shrink"): ("sgmv_tc.cu", "lora_kernels.cu", "ptx.cuh", "internal.h"),
+    ("logits", "expand"): ("lora_kernels.cu", "ptx.cuh", "internal.h"),
+    ("logits", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
 }
 
 

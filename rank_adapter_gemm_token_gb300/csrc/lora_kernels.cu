@@ -11,13 +11,13 @@
 // Shrink works per pair-block (at most 16 pairs of one slot, from the sorted metadata) and K
 // split: each lane streams its share of A[slot] once with 16-byte loads, reusing each vector
 // for the pairs of the block, and writes unscaled fp32 partial sums per split. Expand adds the
-// splits in a fixed order and multiplies by the pair's scale times the slot factor. With one slot per token it works per pair-block and
-// 512-column range: B[slot] rows are read once per block (thread = output column, so both
+// splits in a fixed order and multiplies by the pair's scale times the slot factor. With one
+// slot per token it works per pair-block and column range (512 columns, more when there are
+// enough items): B[slot] rows are read once per block (thread = output column, so both
 // the B rows and y are accessed coalesced) and each y element receives exactly one update.
 // With several slots per token it works per token, adding the slots in order j = 0..J-1.
 // Either way every output is a fixed sequence of fp32 operations (deterministic), tokens
 // whose slots are all -1 are never touched, and with no active pair no block does any work.
-#include "expand_vfull.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -26,7 +26,8 @@ namespace {
 
 constexpr int kShrinkThreads = 256;      // 8 warps; warp w owns adapter rows w, w + 8, ...
 constexpr int kExpandThreads = 256;      // one output column per thread, coalesced B rows and y
-constexpr int kExpandColsPerItem = 512;  // two columns per thread per item
+constexpr int kExpandColsPerItem = 512;  // output columns per item (two per thread) ...
+constexpr int kExpandMaxColsPerItem = 4096;   // ... doubled up to this while the items still fill the SMs
 
 __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
   float s = ptx::bf16_lo(a.x) * ptx::bf16_lo(b.x);
@@ -148,7 +149,7 @@ __device__ __forceinline__ float pair_v(const MetaView& m, int R, int n_ks, int 
 // updates y[t][o] for every token of the block (consecutive o, coalesced). Each y element is
 // updated by exactly one pair, so the result is deterministic.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk,
+lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk, int cols,
                            int skip_fused) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
@@ -173,7 +174,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
       if (q == 0) tok[pi] = done ? -1 : p;          // J == 1: token index == pair index
     }
     __syncthreads();
-    for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
+    for (int o = dc * cols + threadIdx.x; o < min(D, (dc + 1) * cols);
          o += kExpandThreads) {
       const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
       float d[kPairBlock];
@@ -195,7 +196,8 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
 // J > 1: item = (token, 512-column range); slots are added in order j = 0..J-1 so every output
 // is a fixed sequence of fp32 additions. Thread c owns column o: B rows and y coalesced.
 __global__ void __launch_bounds__(kExpandThreads)
-lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk, int skip_fused) {
+lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_ks, int n_dchunk, int cols,
+                         int skip_fused) {
   __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
@@ -221,7 +223,7 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
       vs[j][q] = ss[j] >= 0 ? pair_v(m, R, n_ks, t * J + j, q, rs[j], cs[j]) : 0.f;
     }
     __syncthreads();
-    for (int o = dc * kExpandColsPerItem + threadIdx.x; o < min(D, (dc + 1) * kExpandColsPerItem);
+    for (int o = dc * cols + threadIdx.x; o < min(D, (dc + 1) * cols);
          o += kExpandThreads) {
       float acc = y[static_cast<size_t>(t) * D + o];
       for (int j = 0; j < J; ++j) {
@@ -234,40 +236,6 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
       }
       y[static_cast<size_t>(t) * D + o] = acc;
     }
-  }
-}
-
-// ---------------------------------------------------------------------------------------------
-// Expand after the small-batch fused GEMM, which leaves v of every token against every active
-// slot in vfull[t][a][q]. These kernels are programmatic dependents of that GEMM: everything
-// that does not depend on it (the step's metadata, the B rows, which are prefetched into L2) is
-// done before griddepcontrol.wait, and only v and y are touched after it.
-
-// One slot per token: item = (pair-block, 512-column range), as in lora_expand_segment_kernel.
-__global__ void __launch_bounds__(kExpandThreads)
-lora_expand_vfull_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
-  __shared__ ExpandSmem es;
-  const int items = m.counts[2] * n_dchunk;
-  bool waited = false;
-  for (int item = blockIdx.x; item < items; item += gridDim.x)
-    expand_vfull_segment_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
-  if (!waited) {
-    ptx::grid_dependency_wait();
-    ptx::grid_dependents_launch();
-  }
-}
-
-// Several slots per token: item = (token, 512-column range), slots added in order j = 0..J-1.
-__global__ void __launch_bounds__(kExpandThreads)
-lora_expand_vfull_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n_dchunk) {
-  __shared__ ExpandSmem es;
-  const int items = m.T * n_dchunk;
-  bool waited = false;
-  for (int item = blockIdx.x; item < items; item += gridDim.x)
-    expand_vfull_token_item<kExpandThreads>(y, pool, m, item, n_dchunk, es, &waited);
-  if (!waited) {
-    ptx::grid_dependency_wait();
-    ptx::grid_dependents_launch();
   }
 }
 
@@ -309,39 +277,22 @@ cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
-  const int n_dchunk = (pool.D + kExpandColsPerItem - 1) / kExpandColsPerItem;
+  // Wider column ranges per item amortise an item's set-up (its pairs, their v) over more columns;
+  // they are used while the items still number at least eight per SM (pair-blocks counted as
+  // full, a lower bound, for one slot per token).
+  const long lo_rows = m.J == 1 ? (m.n + kPairBlock - 1) / kPairBlock : m.T;
+  int cols = kExpandColsPerItem;
+  while (cols < kExpandMaxColsPerItem && lo_rows * ((pool.D + 2 * cols - 1) / (2 * cols)) >= 8L * num_sms) cols *= 2;
+  const int n_dchunk = (pool.D + cols - 1) / cols;
   const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
   int grid = num_sms * 8;
   if (grid > max_items) grid = max_items;
   note_launch_begin(kKindExpand, s);
   if (m.J == 1)
-    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip);
+    lora_expand_segment_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, cols, skip);
   else
-    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, skip);
+    lora_expand_token_kernel<<<grid, kExpandThreads, 0, s>>>(y, pool, m, n_ks, n_dchunk, cols, skip);
   cudaError_t e = cudaGetLastError();
-  note_launch_end(kKindExpand, s);
-  return e;
-}
-
-cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
-                                     cudaStream_t s) {
-  if (m.n == 0 || pool.D == 0) return cudaSuccess;
-  const int n_dchunk = (pool.D + kExpandVfullCols - 1) / kExpandVfullCols;
-  const int max_items = (m.J == 1 ? m.n : m.T) * n_dchunk;
-  int grid = num_sms * 8;
-  if (grid > max_items) grid = max_items;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kExpandThreads, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  note_launch_begin(kKindExpand, s);
-  cudaError_t e = (m.J == 1) ? cudaLaunchKernelEx(&cfg, lora_expand_vfull_segment_kernel, y, pool, m, n_dchunk)
-                             : cudaLaunchKernelEx(&cfg, lora_expand_vfull_token_kernel, y, pool, m, n_dchunk);
   note_launch_end(kKindExpand, s);
   return e;
 }
