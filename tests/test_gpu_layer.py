@@ -154,15 +154,15 @@ def test_prefill_config_full_size(cuda_device):
     dw.close()
 
 
-@pytest.mark.parametrize("T,J", [(256, 2), (1024, 2), (256, 1)])
+@pytest.mark.parametrize("T,J", [(256, 2), (1024, 2), (256, 1), (1, 2), (7, 1)])
 def test_lm_head_router_mixture(cuda_device, T, J):
     """The side path on the LM head (hidden 4096 -> a 32000-entry vocabulary) with router-weighted
     mixtures: two adapters per token with per-token gate weights ("[RFC] Per-request activation
     of multiple LoRA adapters", related work: router-driven mixtures; "[vLLM] LoRA",
     add_lora_logits: the LM head takes the same shrink and expand). A 32000-wide output has
     more 128-column blocks than SMs, so both batch sizes take the tiled GEMM with the separate
-    shrink and expand of a 32-wide pool; J = 1 takes the slot-sorted expand, J = 2 the per-token
-    one."""
+    shrink and expand of a 32-wide pool (T = 1 and 7: a single 128-row tile, one-CTA GEMM); J = 1
+    takes the slot-sorted expand, J = 2 the per-token one."""
     wl = synth.logits(T=T, vocab=32000, J=J)
     dw = DeviceWorkload(wl)
     dw.run()
