@@ -508,7 +508,7 @@ def run_ours(args):
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
-    algo = algorithmic_bytes(wl)
+    algo = algorithmic_bytes(wl, torch.cuda.get_device_properties(device).multi_processor_count)
     kinds = {k: v for k, v in trace.items() if v[0] > 0}
     dom = max(kinds, key=lambda k: kinds[k][1])
     n_launch, tot_ms = kinds[dom]
