@@ -190,14 +190,15 @@ MLORA_API mlora_status mlora_base_gemm(const mlora_bf16* x, const mlora_bf16* W,
 MLORA_API mlora_status mlora_lora_shrink(mlora_pool_t pool, mlora_meta_t meta, const mlora_bf16* x, void* stream);
 MLORA_API mlora_status mlora_lora_expand(mlora_pool_t pool, mlora_meta_t meta, float* y, void* stream);
 
-/* Tile choice of the base GEMM for batches of more than 256 tokens (process-wide; no
- * counterpart on the pages: a tuning control). The default, 0, picks per shape: the CTA-pair
- * kernel (tcgen05 cta_group::2, 256 x N tiles with N in {256, 224, 192, 128} chosen so that the
- * tiles fill the resident CTA pairs in whole waves) when the shape has at least one 256 x 256
- * tile per resident pair, else the one-CTA kernel. -1 never uses the pair kernel; 256, 224,
- * 192 or 128 always uses it with that N. Other values: MLORA_ERR_INVALID_ARG, nothing
- * changed. Results differ between choices only by fp32 summation order. Set it between
- * steps, not while a captured graph that launches the GEMM may be re-captured. */
+/* Tile choice of the tiled base GEMM (batches of more than 256 tokens, and smaller batches
+ * whose output is wider than one wave of 128-column blocks; process-wide; no counterpart on the
+ * pages: a tuning control). The default, 0, picks per shape: the CTA-pair kernel (tcgen05
+ * cta_group::2, 256 x N tiles with N in {256, 224, 192, 128} chosen by estimated time: whole
+ * waves of the resident CTA pairs times a per-tile time) whenever the batch spans two or more
+ * 128-row tiles, else the one-CTA kernel. -1 never uses the pair kernel; 256, 224, 192 or 128
+ * always uses it with that N. Other values: MLORA_ERR_INVALID_ARG, nothing changed. Results
+ * differ between choices only by fp32 summation order. Set it between steps, not while a
+ * captured graph that launches the GEMM may be re-captured. */
 MLORA_API mlora_status mlora_set_gemm_tile_n(int n);
 
 /* Allocation-free LoRA side path (no counterpart on the pages: an addition for callers that
