@@ -1,18 +1,26 @@
 """Benchmark of the multi-LoRA batched linear layer on GB300.
 
-Workload (default): the decode batch of the pages' shapes -- 256 tokens at hidden 4096
-through four q/k/v/o-shaped 4096 -> 4096 bf16 linears, each with its own pool of 100
-resident rank-16 adapters (alpha 32); per-token slot uniform over the 100 with 10 % of
-tokens on the sentinel -1. One step = build the slot metadata once, then the four
-linears (base GEMM + shrink + expand each). Metric: tokens per second through the step.
+Workload (default): the mixed serving step -- a Llama-style stack of 32 layers x {qkv
+4096 -> 6144, o 4096 -> 4096, gate_up 4096 -> 28672, down 14336 -> 4096} in bf16, 1024 tokens
+(4 prefill segments of 192 tokens, one adapter each, then 256 decode tokens, one request
+each), tenants Zipf(1.1) over 1000 registered adapters of ranks 8/16/64 admitted into 128 GPU
+slots. One step = build the slot metadata once, then every linear (base GEMM + shrink +
+expand). Metric: tokens per second through the step. Other workloads (decode, prefill,
+compose, logits, tiny) are behind --workload.
 
-Output: one JSON line (rank 0). Kernel durations for the roofline come from a second
-pass of the same K steps with per-kernel CUDA events (the library's trace), so that the
-events do not slow the headline timing. L2 is flushed (256 MiB write) before every timed
-step, outside the timed events.
+Output: one JSON line (rank 0). Kernel durations for the roofline come from a second pass of
+the same steps with per-kernel CUDA events (the library's trace), so that the events do not
+slow the headline timing. L2 is flushed (256 MiB write) before every timed step, outside the
+timed events. The line also carries the step split into its phases (the prefill tokens alone
+and the decode tokens alone, each against its own bound), the adapter load rate (host to
+device, per slot) and the end-to-end rate through the C ABI with host buffers.
 
 --impl reference times the fp64 CPU oracle (the only reference this subject has) on a
 bounded sample of the same workload on the host cores.
+
+--gpus N (N > 1) runs one replica of the workload per GPU (tokens are independent rows; no
+collective on the data path): launched under torchrun it takes WORLD_SIZE ranks, started
+directly it starts torchrun itself.
 """
 from __future__ import annotations
 
@@ -20,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import subprocess
 import sys
 import time
@@ -32,6 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "LoRA-linear tokens/s (1×GB300) + % of HBM / bf16 tensor roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOADS = ("mixed", "decode", "compose", "prefill", "tiny", "logits")
 
 
 def load_peaks():
@@ -47,6 +57,16 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def headline_fields(ms_local: float, tokens_per_rank: int) -> dict:
+    """The line's whole-job fields from this rank's mean step time: the slowest rank's time and
+    the tokens of all ranks over it (one replica per rank)."""
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    ms, value = aggregate_over_ranks(ms_local, tokens_per_rank)
+    return {"value": value, "n_gpus": ws, "ms_per_step": ms, "scaling": "weak",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
 
 
 def aggregate_over_ranks(ms_local: float, tokens_per_rank: int) -> tuple:
@@ -65,30 +85,24 @@ def aggregate_over_ranks(ms_local: float, tokens_per_rank: int) -> tuple:
 
 
 # ------------------------------------------------------------------------------ workload
-def make_workload(name: str):
+def make_workload(name: str, layers: int = 32):
     import synth
-    if name == "decode":
-        return synth.decode()
-    if name == "logits":
-        return synth.logits()
-    if name == "compose":
-        return synth.compose()
-    if name == "tiny":
-        return synth.tiny()
-    if name == "prefill":
-        return synth.prefill()
     if name == "mixed":
-        return synth.mixed()
-    raise SystemExit(f"unknown workload {name}")
+        return synth.mixed(n_layers=layers)
+    return {"decode": synth.decode, "logits": synth.logits, "compose": synth.compose, "tiny": synth.tiny,
+            "prefill": synth.prefill}[name]()
 
 
 def workload_config(wl, name: str) -> dict:
     lin = wl.linears
+    if len(lin) <= 8:
+        what = ", ".join(f"{l.name} {l.K}->{l.D}" for l in lin)
+    else:
+        what = f"{len(lin) // 4} layers x 4 linears (" + ", ".join(
+            f"{l.name.split('.')[-1]} {l.K}->{l.D}" for l in lin[:4]) + ")"
+    phases = "".join(f", {b - a} {n}" for n, a, b in getattr(wl, "phases", []))
     return {
-        "workload": f"{name}: T={wl.T} tokens, J={wl.J}, linears "
-                    + (", ".join(f"{l.name} {l.K}->{l.D}" for l in lin) if len(lin) <= 8 else
-                       f"{len(lin) // 4} layers x (" + ", ".join(f"{l.name.split('.')[-1]} {l.K}->{l.D}" for l in lin[:4]) + ")")
-                    + f", {wl.n_slots} slots r_max={wl.r_max}",
+        "workload": f"{name}: {wl.T} tokens{phases}, J={wl.J}, linears {what}, {wl.n_slots} slots r_max={wl.r_max}",
         "tokens_per_step": wl.T,
         "linears": len(lin),
         "slots": wl.n_slots,
@@ -98,58 +112,84 @@ def workload_config(wl, name: str) -> dict:
     }
 
 
-def algorithmic_bytes(wl, num_sms: int = 152) -> dict:
-    """Bytes each kernel kind must move per step (unique data, each counted once), by path.
+def sub_workload(wl, r0: int, r1: int):
+    """The same linears and adapters over token rows [r0, r1) (a phase of the step)."""
+    import copy
+    sub = copy.copy(wl)
+    sub.T = r1 - r0
+    sub.token_slots = wl.token_slots[r0:r1]
+    sub.scales = None if wl.scales is None else wl.scales[r0:r1]
+    sub.xs = {k: v[r0:r1] for k, v in wl.xs.items()}
+    sub.phases = []
+    return sub
 
-    Small batches (T <= 256 and every output's 128-column blocks within one wave of the SMs: one
-    split-K tensor-core kernel computes the base product and the shrink of every active slot): base_gemm = W + x + y write (fp32) + A rows of the active slots
-    (R rows each, the pool's padded rank) + v write (T x active slots x R, fp32); expand = B rows
-    of the active slots at the true rank padded to 8 + read and write of y rows with an active
-    slot + v reads of the active pairs.
-    Larger batches with rank width 64, 128-token tiles of at most four slots (tensor-core path):
-    shrink = A rows (64 per slot) + x rows of those tiles + the scaled bf16 v tiles written;
-    base_gemm = W + x + y + those v tiles read again + B rows (64 columns per slot). Pairs in
-    tiles with more slots, and every pair of other larger batches: shrink = A rows at the true
-    rank + x rows of active tokens + v partial writes; expand = B rows + y read-modify-write +
-    v reads.
-    Flops: 2*T*K*D per linear for the base product."""
+
+def layer_path(wl, lin, num_sms: int = 152) -> str:
+    """Which kernels the library runs for this linear: 'small' (T <= 256, one rank width, output
+    column blocks within one wave: split-K GEMM with the shrink folded in, then a separate expand)
+    or 'tc' (shrink on the tensor cores, expand inside the base GEMM as extra K blocks)."""
+    classes = getattr(wl, "classes", None)
+    if wl.T <= 256 and not classes and (lin.D + 127) // 128 <= num_sms:
+        return "small"
+    return "tc"
+
+
+def algorithmic(wl, num_sms: int = 152) -> dict:
+    """Bytes and flops the method must move and do per step (each tensor counted once, adapters
+    at their true rank), attributed to the kernel that moves them.
+
+    Per linear: W [D, K] + x [T, K] (bf16) and the fp32 output y [T, D]; the A rows and B rows of
+    every adapter that at least one token uses, at its true rank; v (fp32, one value per active
+    pair and rank row) written by the shrink and read by the expand. Where the expand runs as its
+    own kernel after the GEMM ('small' path) it also reads and writes y on the rows that have an
+    active slot; where it runs inside the base GEMM ('tc' path) y is written once.
+    Flops: 2 T K D for the base product, 2 r K per active pair for the shrink, 2 r D per active
+    pair for the expand.
+    Attribution: 'small': base_gemm = W + x + y + A rows + v write, expand = B rows + y
+    read-modify-write + v read. 'tc': shrink = A rows + x rows of the tokens with an active slot
+    + v write, base_gemm = W + x + y + B rows + v read."""
     slots = wl.token_slots
     active = slots >= 0
-    R = (wl.r_max + 7) // 8 * 8
-    small = wl.T <= 256 and all((l.D + 127) // 128 <= num_sms for l in wl.linears)
-    tensor_core = wl.T > 256 and R == 64
-    fused = np.zeros_like(active)
-    tile_slots = []                                   # distinct slots of each fused 128-token tile
-    if tensor_core:
-        for t0 in range(0, wl.T, 128):
-            d = set(int(s) for s in slots[t0:t0 + 128][active[t0:t0 + 128]])
-            if len(d) <= 4:
-                fused[t0:t0 + 128] = active[t0:t0 + 128]
-                tile_slots.append((min(128, wl.T - t0), d))
-    rest = active & ~fused
-    act_rows = int(np.any(rest, axis=1).sum())
-    pairs = int(rest.sum())
-    distinct = sorted(set(int(s) for s in slots[rest]))
-    tc_slots = sorted(set().union(*(d for _, d in tile_slots))) if tile_slots else []
-    tc_rows = sum(rows for rows, d in tile_slots if d)
-    tc_vtile = sum(rows * len(d) * 64 * 2 for rows, d in tile_slots)
-    out = {"base_gemm": 0, "shrink": 0, "expand": 0, "base_flops": 0, "meta": wl.T * wl.J * 4 * 6}
+    rows = int(np.any(active, axis=1).sum())
+    distinct = sorted(set(int(s) for s in slots[active]))
+    out = {k: 0 for k in ("meta", "base_gemm", "shrink", "expand")}
+    flops = {k: 0 for k in ("base_gemm", "shrink", "expand")}
+    out["meta"] = wl.T * wl.J * 4 * 6
     for l in wl.linears:
-        out["base_gemm"] += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
-        out["base_flops"] += 2 * wl.T * l.K * l.D
-        ra = sum(l.adapters[s].rank for s in distinct)
-        rb = sum((l.adapters[s].rank + 7) // 8 * 8 for s in distinct)
-        if small:
-            out["base_gemm"] += len(distinct) * R * l.K * 2 + wl.T * len(distinct) * R * 4
-            out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
-            continue
-        if tc_slots:
-            out["shrink"] += len(tc_slots) * 64 * l.K * 2 + tc_rows * l.K * 2 + tc_vtile
-            out["base_gemm"] += tc_vtile + len(tc_slots) * 64 * l.D * 2
-        if pairs:
-            out["shrink"] += ra * l.K * 2 + act_rows * l.K * 2 + pairs * R * 4
-            out["expand"] += rb * l.D * 2 + act_rows * l.D * 8 + pairs * R * 4
+        ranks = {s: l.adapters[s].rank for s in distinct}
+        sum_r = sum(ranks.values())
+        pair_r = int(sum(ranks[int(s)] for s in slots[active]))
+        v = pair_r * 4
+        base = l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
+        a_rows, b_rows = sum_r * l.K * 2, sum_r * l.D * 2
+        f_base, f_shrink, f_expand = 2 * wl.T * l.K * l.D, 2 * pair_r * l.K, 2 * pair_r * l.D
+        if layer_path(wl, l, num_sms) == "small":
+            out["base_gemm"] += base + a_rows + v
+            out["expand"] += b_rows + rows * l.D * 8 + v
+            flops["base_gemm"] += f_base + f_shrink
+            flops["expand"] += f_expand
+        else:
+            out["shrink"] += a_rows + rows * l.K * 2 + v
+            out["base_gemm"] += base + b_rows + v
+            flops["shrink"] += f_shrink
+            flops["base_gemm"] += f_base + f_expand
+    out["flops"] = flops
     return out
+
+
+def roofline_of(byts: float, flops: float, seconds: float, peaks: dict) -> dict:
+    """A kernel (or step) against the roofline: bound by whichever of bytes / HBM peak and
+    flops / bf16 peak takes longer."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    bound = "tensor" if flops / tc > byts / hbm else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = flops / seconds / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = byts / seconds / 1e9, peaks["hbm_gbs"], "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "bound_us": max(flops / tc, byts / hbm) * 1e6, "hbm_frac": byts / hbm / seconds,
+            "tensor_frac": flops / tc / seconds}
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -223,24 +263,29 @@ class ClockSampler:
 # ------------------------------------------------------------------------------ oracle timing
 def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
     """Times the fp64 oracle on a bounded sample of the workload: all linears of the step for a
-    growing number of token rows until about budget_s of CPU work. Returns tokens/s, rows, threads."""
+    growing number of token rows until about budget_s of CPU work. A step whose tensors are
+    generated on demand (the mixed step) is timed on its first layer and the time scaled to all
+    layers (every layer has the same shapes and adapter set). Returns (tokens/s, rows, threads,
+    seconds per step for those rows, extrapolated)."""
     import oracle
+    import synth
     threads = oracle.default_threads()
     T = wl.T
-    # a step whose tensors are generated on demand (the mixed step): time its first layer and
-    # scale to all layers (every layer has the same shapes and adapter set)
     scale = 1.0
-    if any(l.W is None for l in wl.linears):
-        first = wl.linears[:len(synth_modules())]
+    lazy = any(l.W is None for l in wl.linears)
+    if lazy:
+        first = wl.linears[:len(synth.MIXED_MODULES)]
         scale = len(wl.linears) / len(first)
         if getattr(wl, "_first_layer", None) is None:     # generated once per workload object
-            wl._first_layer = type(wl)(wl.name, wl.seed, wl.T, wl.J, wl.n_slots, wl.r_max, wl.token_slots,
-                                       wl.scales, {l.x_id: synth_x(wl, l) for l in first},
-                                       [synth_materialize(wl, l) for l in first])
+            import copy
+            fl = copy.copy(wl)
+            fl.xs = {l.x_id: synth.materialize_x(wl, l) for l in first}
+            fl.linears = [synth.materialize_linear(wl, l) for l in first]
+            wl._first_layer = fl
         wl = wl._first_layer
     cap = T if max_rows is None else min(T, max_rows)
     rows_n = min(cap, max(1, threads))
-    spent, tokens = 0.0, 0
+    spent = 0.0
     rng = np.random.default_rng(0)
     while True:
         rows = np.sort(rng.choice(T, size=rows_n, replace=False))
@@ -250,35 +295,20 @@ def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
                           rows=rows, threads=threads)
         real = time.perf_counter() - t0
         spent += real
-        tokens = rows_n
         last = real * scale
         if rows_n >= cap or spent + real * 2.5 > budget_s:
             break
         rows_n = min(cap, rows_n * 2)
-    return tokens / last, tokens, threads, last
+    return rows_n / last, rows_n, threads, last, lazy
 
 
-def synth_modules():
+def sample_note(wl, rows, seconds=None, lazy=False) -> str:
     import synth
-    return synth.MIXED_MODULES
-
-
-def synth_x(wl, lin):
-    import synth
-    return synth.materialize_x(wl, lin)
-
-
-def synth_materialize(wl, lin):
-    import synth
-    return synth.materialize_linear(wl, lin)
-
-
-def sample_note(wl, rows, seconds=None) -> str:
-    lazy = any(l.W is None for l in wl.linears)
-    what = (f"{rows} of {wl.T} token rows through the first {len(synth_modules())} of {len(wl.linears)} "
-            f"linears, time scaled to all of them" if lazy else
+    what = (f"{rows} of {wl.T} token rows through the first {len(synth.MIXED_MODULES)} of {len(wl.linears)} "
+            f"linears, time extrapolated to all of them" if lazy else
             f"{rows} of {wl.T} token rows through all {len(wl.linears)} linears")
-    return what + (f" ({seconds:.1f} s)" if seconds is not None else " per step")
+    return what + (f" ({seconds:.1f} s per step, extrapolated)" if seconds is not None and lazy else
+                   f" ({seconds:.2f} s per step)" if seconds is not None else " per step")
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -286,12 +316,14 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, args.layers)
     step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     rows = None
     times = []
+    lazy = False
+    threads = 1
     for i in range(args.warmup + args.steps):
-        tps, rows, threads, dt = oracle_sample(wl, budget_s=step_budget, max_rows=rows)
+        _, rows, threads, dt, lazy = oracle_sample(wl, budget_s=step_budget, max_rows=rows)
         if i >= args.warmup:
             times.append(dt)
     ms = 1000.0 * float(np.mean(times))
@@ -302,7 +334,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
         "config": workload_config(wl, args.workload),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample_note(wl, rows)},
+                         "sample": sample_note(wl, rows, lazy=lazy), "extrapolated": lazy},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -312,11 +344,12 @@ def run_reference(args):
 # ------------------------------------------------------------------------------ our arm
 # Sources each recorded kernel is built from; a traffic record holds only while they are unchanged.
 KERNEL_SOURCES = {
+    ("mixed", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
+    ("mixed", "shrink"): ("shrink_tc.cu", "ptx.cuh", "internal.h"),
     ("decode", "base_gemm"): ("gemm_tc.cu", "ptx.cuh", "internal.h"),
     ("decode", "expand"): ("expand_vfull.cu", "expand_vfull.cuh", "ptx.cuh", "internal.h"),
     ("prefill", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
-    ("prefill", "shrink"): ("sgmv_tc.cu", "lora_kernels.cu", "ptx.cuh", "internal.h"),
-    ("logits", "expand"): ("lora_kernels.cu", "ptx.cuh", "internal.h"),
+    ("prefill", "shrink"): ("shrink_tc.cu", "ptx.cuh", "internal.h"),
     ("logits", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
 }
 
@@ -347,6 +380,62 @@ def recorded_traffic(kind: str, workload: str):
     return r.get("dram_bytes_per_launch")
 
 
+def time_graph(run, steps: int, warmup: int, stream, flush, device, barrier):
+    """Captures run() once into a CUDA graph and times `steps` replays (L2 flushed before each)
+    with CUDA events on `stream`; returns (ms per replay, graph)."""
+    import torch
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        run()                                  # first use on the capture stream, outside the capture
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        run()
+    torch.cuda.synchronize(device)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        graph.replay()
+        ends[i].record(stream)
+    barrier()
+    return float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)])), graph
+
+
+def time_adapter_loads(dw, n_slots: int = 16):
+    """Host-to-device adapter load rate: re-loads up to n_slots resident adapters of the largest
+    linear from pinned host buffers (the pinning done beforehand) and times the queued copies until
+    the pool's loads are complete (wall clock)."""
+    import torch
+    import synth
+    from rank_adapter_gemm_token_gb300 import mlora
+    dl = max(dw.linears, key=lambda d: d.lin.K + d.lin.D)
+    lin = dl.lin
+    staged = []
+    for s, ad in sorted(lin.adapters.items())[:n_slots]:
+        if isinstance(ad, synth.LazyAdapter):
+            ad = ad.materialize(lin.K, lin.D)
+        a = torch.from_numpy(np.ascontiguousarray(ad.A).view(np.int16)).pin_memory()
+        b = torch.from_numpy(np.ascontiguousarray(ad.B).view(np.int16)).pin_memory()
+        staged.append((s, a, b, ad))
+    torch.cuda.synchronize()
+    nbytes = sum(a.numel() * 2 + b.numel() * 2 for _, a, b, _ in staged)
+    t0 = time.perf_counter()
+    for s, a, b, ad in staged:
+        mlora.mlora_load_adapter(dl.pool.handle, s, a.data_ptr(), b.data_ptr(), ad.rank, ad.alpha, ad.rslora)
+    dl.pool.sync()
+    dt = time.perf_counter() - t0
+    return {"linear": f"{lin.name} {lin.K}->{lin.D}", "slots": len(staged), "bytes": nbytes,
+            "ms_per_slot": 1000.0 * dt / max(1, len(staged)), "h2d_GBps": nbytes / dt / 1e9,
+            "how": "mlora_load_adapter from pinned host memory on the pool's copy stream, wall clock until "
+                   "mlora_pool_sync returns (slot zeroing, A copy, strided B copy, slot factor)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -358,14 +447,19 @@ def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local)) if "device_id" in \
-            dist.init_process_group.__code__.co_varnames else dist.init_process_group("nccl")
+        if "device_id" in dist.init_process_group.__code__.co_varnames:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("nccl")
     device = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(device)
     __graft_entry__.build()
 
-    wl = make_workload(args.workload)
+    t_setup = time.perf_counter()
+    wl = make_workload(args.workload, args.layers)
     dw = DeviceWorkload(wl, device=device)
+    torch.cuda.synchronize(device)
+    setup_s = time.perf_counter() - t_setup
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
 
@@ -384,54 +478,54 @@ def run_ours(args):
     kernels_per_step = mlora.mlora_launch_count() - l0
     barrier()
 
-    # The step (metadata build + every linear) is captured once into a CUDA graph and replayed:
-    # the same kernels with the same arguments, without per-call host work.
-    run_step = lambda: dw.run(stream)  # noqa: E731
-    graph = None
-    if not args.no_graph:
-        cap = torch.cuda.Stream(device)
-        with torch.cuda.stream(cap):
-            dw.run()                      # first use on the capture stream, outside the capture
-        torch.cuda.synchronize(device)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            dw.run()
-        torch.cuda.synchronize(device)
-        run_step = graph.replay
-        for _ in range(args.warmup):
-            flush.zero_()
-            run_step()
-        barrier()
-
-    # ---- headline: K timed steps, L2 flushed before each, no tracing
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- headline: K timed steps, L2 flushed before each, no tracing. The step (metadata build +
+    # every linear) is captured once into a CUDA graph and replayed: the same kernels with the same
+    # arguments, without per-call host work.
     clocks = ClockSampler(local)
     clocks.start()
-    launches0 = mlora.mlora_launch_count()
-    barrier()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        run_step()
-        ends[i].record(stream)
-    barrier()
+    if args.no_graph:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            dw.run(stream)
+            ends[i].record(stream)
+        barrier()
+        ms_local = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+    else:
+        ms_local, _ = time_graph(lambda: dw.run(), args.steps, args.warmup, stream, flush, device, barrier)
     wall = time.perf_counter() - wall0
-    launches = mlora.mlora_launch_count() - launches0 if graph is None else kernels_per_step * args.steps
     clock_info = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms, value = aggregate_over_ranks(float(np.mean(step_ms)), wl.T)
+    launches = kernels_per_step * args.steps
+    head = headline_fields(ms_local, wl.T)
 
-    # ---- per-kernel durations: the same K steps again with the library's event trace
-    trace_steps = min(args.steps, 100)
+    # ---- per-kernel durations: the same steps again with the library's event trace
+    trace_steps = min(args.steps, 20)
     mlora.mlora_trace_enable(int(kernels_per_step) * trace_steps + 64)
-    for i in range(trace_steps):
+    for _ in range(trace_steps):
         flush.zero_()
         dw.run(stream)
     barrier()
     trace = mlora.mlora_trace_read()
     mlora.mlora_trace_disable()
+
+    # ---- phases: the prefill tokens alone and the decode tokens alone, through the same linears
+    peaks, peak_src = load_peaks()
+    num_sms = torch.cuda.get_device_properties(device).multi_processor_count
+    phases = {}
+    for name, r0, r1 in getattr(wl, "phases", []):
+        sub = dw.sub_rows(r0, r1)
+        p_ms, _ = time_graph(lambda: sub.run(), max(3, min(args.steps, 20)), 3, stream, flush, device, barrier)
+        sw = sub_workload(wl, r0, r1)
+        pa = algorithmic(sw, num_sms)
+        rf = roofline_of(sum(v for k, v in pa.items() if k != "flops"), sum(pa["flops"].values()), p_ms / 1000.0, peaks)
+        phases[name] = {"tokens": r1 - r0, "us": p_ms * 1000.0, "bound": rf["bound"], "bound_us": rf["bound_us"],
+                        "frac": rf["bound_us"] / (p_ms * 1000.0), "hbm_frac": rf["hbm_frac"],
+                        "tensor_frac": rf["tensor_frac"]}
+        sub.close()
 
     # ---- end to end: pinned host inputs in, step, result out, every step
     xs_host = {k: v.cpu().pin_memory() for k, v in dw.x.items()}
@@ -489,7 +583,7 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
-    for i in range(args.steps):
+    for _ in range(max(3, min(args.steps, 20))):
         flush.zero_()
         e_start.record(stream)
         e2e_run()
@@ -500,66 +594,64 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     dw.meta.status()
 
+    load_rate = time_adapter_loads(dw)
+
     if rank != 0:
         if ws > 1:
             dist.barrier()
             dist.destroy_process_group()
+        dw.close()
         return 0
 
     # ---- roofline of the dominant kernel
-    peaks, peak_src = load_peaks()
-    algo = algorithmic_bytes(wl, torch.cuda.get_device_properties(device).multi_processor_count)
+    algo = algorithmic(wl, num_sms)
     kinds = {k: v for k, v in trace.items() if v[0] > 0}
     dom = max(kinds, key=lambda k: kinds[k][1])
     n_launch, tot_ms = kinds[dom]
     avg_s = tot_ms / n_launch / 1000.0
-    launches_per_step = n_launch / trace_steps
-    if dom == "base_gemm":
-        flops = algo["base_flops"] / launches_per_step
-        byts = algo["base_gemm"] / launches_per_step
-        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        bound = "tensor" if flops / byts > ridge else "hbm"
-    else:
-        byts = algo.get(dom, 0) / launches_per_step
-        flops, bound = 0, "hbm"
-    if bound == "tensor":
-        achieved, peak, unit = flops / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = byts / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
-    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
-                if peak_src == "measured" else "fallback",
+    per_step = n_launch / trace_steps
+    rf = roofline_of(algo.get(dom, 0) / per_step, algo["flops"].get(dom, 0) / per_step, avg_s, peaks)
+    roofline = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
+                "unit": rf["unit"], "frac": rf["frac"],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
                 "traffic": recorded_traffic(dom, args.workload),
-                "algorithmic_bytes_per_launch": byts, "avg_launch_us": avg_s * 1e6}
+                "algorithmic_bytes_per_launch": algo.get(dom, 0) / per_step,
+                "algorithmic_flops_per_launch": algo["flops"].get(dom, 0) / per_step,
+                "avg_launch_us": avg_s * 1e6}
     per_kernel = {}
+    total_traced = sum(v[1] for v in kinds.values())
     for k, (n, t) in kinds.items():
         per = n / trace_steps
-        entry = {"launches_per_step": per, "avg_us": 1000.0 * t / n, "share": t / sum(v[1] for v in kinds.values())}
-        if k in algo and algo[k] > 0:
-            entry["achieved_GBps"] = algo[k] / per / (t / n / 1000.0) / 1e9
+        entry = {"launches_per_step": per, "avg_us": 1000.0 * t / n, "share": t / total_traced}
+        kb, kf = algo.get(k, 0) / per, algo["flops"].get(k, 0) / per
+        if kb > 0:
+            entry["achieved_GBps"] = kb / (t / n / 1000.0) / 1e9
             entry["frac_hbm"] = entry["achieved_GBps"] / peaks["hbm_gbs"]
-        if k == "base_gemm":
-            entry["achieved_TFLOPs"] = algo["base_flops"] / per / (t / n / 1000.0) / 1e12
+        if kf > 0:
+            entry["achieved_TFLOPs"] = kf / (t / n / 1000.0) / 1e12
             entry["frac_bf16"] = entry["achieved_TFLOPs"] / peaks["bf16_tflops"]
         per_kernel[k] = entry
     # the whole step against its own bound: the slower of (all algorithmic bytes / HBM peak) and
-    # (all flops / bf16 peak), over the measured step time
-    step_bytes = sum(v for k, v in algo.items() if k not in ("base_flops",))
-    bound_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), algo["base_flops"] / (peaks["bf16_tflops"] * 1e12))
-    step_roofline = {"bound_us": bound_s * 1e6, "frac": bound_s / (ms / 1000.0),
-                     "bytes_per_step": step_bytes, "flops_per_step": algo["base_flops"]}
+    # (all flops / bf16 peak), over the measured step time; and each fraction alone
+    step_bytes = sum(v for k, v in algo.items() if k != "flops")
+    step_flops = sum(algo["flops"].values())
+    srf = roofline_of(step_bytes, step_flops, ms_local / 1000.0, peaks)
+    step_roofline = {"bound": srf["bound"], "bound_us": srf["bound_us"], "frac": srf["bound_us"] / (ms_local * 1000.0),
+                     "hbm_frac": srf["hbm_frac"], "tensor_frac": srf["tensor_frac"],
+                     "bytes_per_step": step_bytes, "flops_per_step": step_flops}
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        tps, rows, threads, dt = oracle_sample(wl, budget_s=args.cpu_budget)
+        tps, rows, threads, dt, lazy = oracle_sample(wl, budget_s=args.cpu_budget)
         cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": sample_note(wl, rows, dt)}
+               "sample": sample_note(wl, rows, dt, lazy), "extrapolated": lazy}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": head["n_gpus"], "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": head["scaling"], "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
-        "config": dict(workload_config(wl, args.workload), parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+        "config": dict(workload_config(wl, args.workload), parallelism=head["parallelism"]),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
@@ -567,9 +659,12 @@ def run_ours(args):
         "clocks": clock_info,
         "kernels": per_kernel,
         "step_roofline": step_roofline,
+        "phases": phases,
+        "adapter_load": load_rate,
+        "setup_s": setup_s,
         "wall_s_timed_region": wall,
         "kernel_timing": f"second pass of {trace_steps} steps with per-kernel CUDA events on the launch stream",
-        "step_launch": "CUDA graph replay of the captured step" if graph is not None else "direct calls",
+        "step_launch": "direct calls" if args.no_graph else "CUDA graph replay of the captured step",
     }
     print(json.dumps(line), flush=True)
     dw.close()
@@ -579,19 +674,37 @@ def run_ours(args):
     return 0
 
 
-def main():
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mlora", choices=["mlora", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "compose", "prefill", "tiny", "mixed", "logits"])
+    ap.add_argument("--workload", default="mixed", choices=WORKLOADS)
+    ap.add_argument("--layers", type=int, default=32, help="layers of the mixed step (a smaller case for captures)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the library directly for every step")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start them under torchrun (rendezvous on the loopback address)
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__),
+               *(sys.argv[1:] if argv is None else argv)]
+        return subprocess.call(cmd)
+    ws = dist_env()[0]
+    if ws != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch one rank per GPU")
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -74,17 +74,43 @@ enum {
 #define MLORA_MAX_SLOTS_PER_TOKEN 8
 #define MLORA_MAX_TOKENS 65535
 #define MLORA_MAX_SLICES 8            /* output slices of one fused linear (mlora_load_adapter_sliced) */
+#define MLORA_MAX_CLASSES 8           /* rank classes of one pool (mlora_pool_create_classes) */
 
 /* ------------------------------------------------------------------ adapter pool ----- */
 
-/* Creates the stacked slot pool of one adapted linear (K inputs, D outputs):
- *   A_pool [n_slots, R, K] and B_pool [n_slots, D, R] bf16, zero-initialised, where
- *   R = r_max rounded up to a multiple of 8; a per-slot factor c (fp32) and true rank.
- * ("Multi-LoRA Serving Explained", max-lora-rank section: slots are zero blocks sized for
- * the maximum rank; a smaller adapter fills the top-left corner.)
+/* Creates the slot pool of one adapted linear (K inputs, D outputs), every slot sized for r_max
+ * ("Multi-LoRA Serving Explained", max-lora-rank section: slots are zero blocks sized for the
+ * maximum rank; a smaller adapter fills the top-left corner).
+ * Layout: the slots' rank rows form one column space of C columns; slot s owns R columns
+ * starting at off_s = s * R (C = n_slots * R), R = the slot width of r_max: 8, 16, 32 or 64 for
+ * r_max up to 64, else r_max rounded up to a multiple of 64 (so no slot straddles a 64-column
+ * block). A_pool [C, K] holds row
+ * off_s + q of slot s's A (row q), B_pool [D, C] holds column off_s + q of slot s's B (column q),
+ * both bf16 and zero beyond each adapter's rank; plus a per-slot factor c (fp32) and true rank.
+ * A 64-column block of that space is what the tensor-core side path multiplies at once.
  * copy_stream: the stream adapter loads run on (NULL: the pool creates its own).
  * The pool allocates with cudaMalloc here and never on the hot path. */
 MLORA_API mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_stream, mlora_pool_t* out);
+
+/* A pool whose slots come in rank classes ("Multi-LoRA Serving Explained", max-lora-rank
+ * section: padding every slot to the largest rank wastes memory; "[vLLM] LoRA" (secrett2633
+ * blog), S-LoRA section: adapters of different ranks served together from one memory pool).
+ * Class c has class_slots[c] slots for adapters of rank at most class_rank[c]; slots are
+ * numbered class by class (class 0 first) and slot i of class c owns w_c columns of the column
+ * space, w_c = the slot width of class_rank[c] (as for mlora_pool_create), right after the
+ * previous slot; each class starts on a multiple of min(w_c, 64) columns. So a rank-8 slot's B
+ * row is 16 bytes and eight such slots share one 64-column block, and the pool holds
+ * C * (K + D) * 2 bytes with C = the end of the last class (mlora_pool_layout).
+ * n_classes in [1, MLORA_MAX_CLASSES], class_slots[c] >= 1 (at most MLORA_MAX_SLOTS in all),
+ * class_rank[c] in [1, MLORA_MAX_RANK]; else MLORA_ERR_INVALID_ARG. Pools used with one metadata
+ * object must have the same classes (MLORA_ERR_MISMATCH otherwise). mlora_pool_create(n, r, ...)
+ * is this call with one class. */
+MLORA_API mlora_status mlora_pool_create_classes(int n_classes, const int* class_slots, const int* class_rank, int K,
+                                                 int D, void* copy_stream, mlora_pool_t* out);
+
+/* The pool's column space: C, and per slot its first column and width (host arrays of n_slots
+ * entries; any pointer may be NULL). */
+MLORA_API mlora_status mlora_pool_layout(mlora_pool_t pool, int* C, int32_t* slot_off, int32_t* slot_width);
 
 /* Waits for this pool's loads and uses to finish, then frees it. NULL is accepted. */
 MLORA_API mlora_status mlora_pool_destroy(mlora_pool_t pool);
@@ -92,11 +118,13 @@ MLORA_API mlora_status mlora_pool_destroy(mlora_pool_t pool);
 /* Copies one adapter into a slot ("LoRA Serving", section 4.1: activating an adapter copies its
  * weights into a free GPU slot; the caller chooses the slot and keeps the id -> slot map).
  *   A_host: [rank, K] bf16 row-major, B_host: [D, rank] bf16 row-major (host memory).
- *   rank <= r_max (else MLORA_ERR_RANK_TOO_LARGE, message naming both ranks), alpha finite.
+ *   rank <= the slot's maximum rank (r_max, or its class's rank; else MLORA_ERR_RANK_TOO_LARGE,
+ *   message naming both ranks), alpha finite.
  *   rslora != 0 selects c = alpha / sqrt(rank), else c = alpha / rank.
  * Runs on the pool's copy stream after every mlora_linear already issued on this pool
- * (write-after-read ordering by event): the slot is zeroed, A is copied to rows 0..rank-1,
- * B to columns 0..rank-1 (row pitch R). Returns when the copies are queued; with pinned
+ * (write-after-read ordering by event): the slot's columns are zeroed, A is copied to rows
+ * off_s .. off_s + rank - 1 of A_pool, B to columns off_s .. of B_pool (a strided copy, row
+ * pitch C). Returns when the copies are queued; with pinned
  * host buffers they are asynchronous and the buffers must stay valid until
  * mlora_pool_sync() or the next mlora_linear on this pool has been ordered after them.
  * With pageable buffers the copy is complete on return. */
@@ -128,21 +156,27 @@ MLORA_API mlora_status mlora_clear_slot(mlora_pool_t pool, int slot);
 /* Blocks until every queued load of this pool has finished. */
 MLORA_API mlora_status mlora_pool_sync(mlora_pool_t pool);
 
-/* Device pointers and sizes of the pool (for inspection and tests; owned by the pool). */
+/* Device pointers and sizes of the pool (for inspection and tests; owned by the pool): r_pad is
+ * the widest slot, A_pool is [C, K] and B_pool [D, C] (mlora_pool_layout gives C and the slots'
+ * columns). */
 MLORA_API mlora_status mlora_pool_info(mlora_pool_t pool, int* n_slots, int* r_pad, int* K, int* D, void** A_pool,
                              void** B_pool, void** slot_scale, void** slot_rank);
 
-/* Bytes of device memory held by a pool's A and B slots: n_slots * R * (K + D) * 2 with
- * R = r_max rounded up to 8 ("Multi-LoRA Serving Explained", memory maths: rank * (in + out)
- * numbers per adapted layer, slots reserved at the maximum rank). 0 for invalid sizes. */
+/* Bytes of device memory held by the A and B slots of mlora_pool_create's pool:
+ * n_slots * R * (K + D) * 2 with R = the slot width of r_max ("Multi-LoRA Serving Explained",
+ * memory maths: rank * (in + out) numbers per adapted layer, slots reserved at the maximum rank).
+ * 0 for invalid sizes. */
 MLORA_API size_t mlora_pool_bytes(int n_slots, int r_max, int K, int D);
 
 /* ------------------------------------------------------------------ step metadata ---- */
 
 /* Creates a metadata object for steps of at most max_tokens tokens and max_slots_per_token
  * (J) adapter slots per token ("[RFC] ...", item 5: max_loras_per_request), for pools whose
- * r_max is at most r_max. Holds the sorted pair order, the segment table, per-pair scales
- * and the shrink workspace (16 * max_tokens * J * r_max fp32, r_max rounded up to 8). */
+ * r_max is at most r_max. Holds the sorted pair order, the segment table, per-pair scales,
+ * the CUDA-core shrink workspace (16 * max_tokens * J * R fp32, R the slot width of r_max) and
+ * the tensor-core side path's unit lists with one 16 KB v tile per unit (units: pairs of an
+ * M-tile of 128 tokens and a 64-column block of the slot space its tokens use; capacity
+ * min(max_tokens * J * ceil(R / 64), tiles * 256, 16384)). */
 MLORA_API mlora_status mlora_meta_create(int max_tokens, int max_slots_per_token, int r_max, mlora_meta_t* out);
 MLORA_API mlora_status mlora_meta_destroy(mlora_meta_t meta);
 
@@ -178,6 +212,10 @@ MLORA_API mlora_status mlora_meta_read(mlora_meta_t meta, int32_t* order, int32_
  *   overwritten. T is the meta's last build. The base product runs on the tensor cores;
  *   when the step has no active pair the LoRA kernels do no work, and rows whose slots are
  *   all -1 equal the base product exactly. Orders itself after the pool's queued loads.
+ * Two paths: small batches of a one-class pool (T <= 256, output column blocks within one wave
+ * of the SMs, few active slots) run the base product and the shrink in one split-K kernel, then
+ * the expand; every other step shrinks on the tensor cores per (M-tile, column block) and adds
+ * the expand inside the base GEMM as extra K blocks (y written once).
  * Calls that share a meta or a pool must be ordered on one stream. */
 MLORA_API mlora_status mlora_linear(mlora_pool_t pool, mlora_meta_t meta, const mlora_bf16* x, const mlora_bf16* W, float* y,
                           void* stream);
@@ -201,24 +239,34 @@ MLORA_API mlora_status mlora_lora_expand(mlora_pool_t pool, mlora_meta_t meta, f
  * captured graph that launches the GEMM may be re-captured. */
 MLORA_API mlora_status mlora_set_gemm_tile_n(int n);
 
+/* Path choice of mlora_linear (process-wide; no counterpart on the pages: a tuning and test
+ * control): 0 automatic (default), 1 the small-batch path whenever the step allows it, 2 always
+ * the tensor-core side path. Other values: MLORA_ERR_INVALID_ARG. Results differ between paths
+ * only by rounding (fp32 summation order; bf16 rounding of the scaled v on the tensor-core
+ * path). Set it between steps. */
+MLORA_API mlora_status mlora_set_path(int path);
+
 /* Allocation-free LoRA side path (no counterpart on the pages: an addition for callers that
  * cannot allocate device memory, such as a serving engine that has handed all free device
  * memory to its KV cache at start-up, so a later cudaMalloc fails, or code on a
  * latency-critical path that cannot accept the implicit device synchronisation of
  * cudaMalloc/cudaFree). It needs no pool or metadata object:
  *   y[t, :] += sum_j s[t,j] * slot_scale[slot] * B_slot (A_slot x[t, :])  for slot = token_slots[t*J + j],
- * over caller-owned device buffers laid out as a pool is (A_pool [n_slots, r_pad, K],
- * B_pool [n_slots, D, r_pad] bf16, zero beyond each slot's rank; slot_scale [n_slots] fp32;
- * slot_rank [n_slots] int32, 0 = empty). scales may be NULL (s = 1). A token slot outside
- * [0, n_slots) or naming an empty slot adds nothing. y must already hold the base product.
+ * over caller-owned device buffers laid out slot by slot (A_pool [n_slots, r_pad, K],
+ * B_pool [n_slots, D, r_pad] bf16, zero beyond each slot's rank -- not the column space of
+ * mlora_pool_create's pools; slot_scale [n_slots] fp32; slot_rank [n_slots] int32, 0 = empty,
+ * at most r_pad). scales may be NULL (s = 1). A token slot outside [0, n_slots), or naming a slot
+ * whose rank is not in [1, r_pad], adds nothing. y must already hold the base product.
  * Its only workspace is a fixed array compiled into the library (4 MiB, held by every GPU
  * that loads it until the process exits), so T * J * r_pad must not exceed 1,048,576
  * (else MLORA_ERR_TOO_MANY_TOKENS, nothing launched). It calls no cudaMalloc, cudaFree or
- * other allocating routine. The first call on each device looks up the workspace's device
- * address (cudaGetSymbolAddress) with that device current; make that first call before any
- * stream capture. All calls share the workspace: calls that overlap on the GPU (different
- * streams, devices aside) race and must be ordered by the caller. Nothing carries over
- * between calls: every workspace value read was written earlier in the same call. */
+ * other allocating routine. The workspace's device address is looked up (cudaGetSymbolAddress)
+ * with the device current on every call made outside stream capture and kept per device; a
+ * call inside a capture uses the kept address, so make the first call on each device (and the
+ * first after a cudaDeviceReset) outside any capture. All calls share the workspace: calls that
+ * overlap on the GPU (different streams, devices aside) race and must be ordered by the
+ * caller. Nothing carries over between calls: every workspace value read was written earlier
+ * in the same call. */
 MLORA_API mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, const int32_t* token_slots,
                                                 const float* scales, int T, int J, const mlora_bf16* A_pool,
                                                 const mlora_bf16* B_pool, const float* slot_scale,

@@ -1,7 +1,6 @@
 // Expand work items after the small-batch fused GEMM, which leaves v of every token against every
 // active slot in MetaView::vfull. Used by the vfull expand kernels (programmatic dependents of
-// the GEMM); the B-row prefetch helper is also called by the GEMM's epilogue warps, and the
-// overflow-window expand (expand_window.cu) shares the shared-memory layout and dot product.
+// the GEMM); the B-row prefetch helper is also called by the GEMM's epilogue warps.
 //
 // y[t][o] += sum_j s c sum_q B_slot[o][q] v[t][slot][q]  ("Multi-LoRA Serving Explained", batched
 // serving: each token's side path added to the shared base product; "[RFC] Per-request
@@ -41,21 +40,21 @@ __device__ __forceinline__ float ev_dot8(const uint4& b, const float* v) {
 // Prefetches into L2 the B rows an item will read (a hint; no ordering needed).
 __device__ __forceinline__ void expand_vfull_prefetch(const PoolView& pool, const MetaView& m, int item,
                                                       int n_dchunk, int tid, int nthreads) {
-  const int D = pool.D, R = pool.R;
+  const int D = pool.D;
   const int dc = item % n_dchunk, key = item / n_dchunk;
   const int oa = dc * kExpandVfullCols, ob = min(D, oa + kExpandVfullCols);
   if (m.J == 1) {
     const int slot = m.blk_slot[key];
     const int rpad = (pool.slot_rank[slot] + 7) & ~7;
     for (int o = oa + tid; o < ob; o += nthreads)
-      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(slot) * D + o) * R + u);
+      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[slot] + u);
   } else {
     for (int j = 0; j < m.J; ++j) {
       const int s = m.pair_slot[key * m.J + j];
       if (s < 0) continue;
       const int rpad = (pool.slot_rank[s] + 7) & ~7;
       for (int o = oa + tid; o < ob; o += nthreads)
-        for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(s) * D + o) * R + u);
+        for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[s] + u);
     }
   }
 }
@@ -82,9 +81,10 @@ __device__ __forceinline__ void expand_vfull_segment_item(float* __restrict__ y,
     es.act[threadIdx.x] = m.pair_act[p];
     es.coef[threadIdx.x] = pool.slot_scale[slot] * m.pair_scale[p];
   }
+  const int boff = pool.slot_off[slot];
   if (!*waited) {
     for (int o = oa + threadIdx.x; o < ob; o += NT)
-      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(slot) * D + o) * R + u);
+      for (int u = 0; u < rpad; u += 32) prefetch_l2(pool.B + static_cast<size_t>(o) * pool.C + boff + u);
   }
   __syncthreads();
   if (!*waited) {
@@ -99,7 +99,7 @@ __device__ __forceinline__ void expand_vfull_segment_item(float* __restrict__ y,
   }
   __syncthreads();
   for (int o = oa + threadIdx.x; o < ob; o += NT) {
-    const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
+    const uint4* brow = reinterpret_cast<const uint4*>(pool.B + static_cast<size_t>(o) * pool.C + boff);
     for (int g = 0; g < cnt; g += 4) {               // pairs in groups of four (few registers)
       float yv[4], d[4];
 #pragma unroll
@@ -145,7 +145,8 @@ __device__ __forceinline__ void expand_vfull_token_item(float* __restrict__ y, c
     for (int j = 0; j < J; ++j)
       if (es.ss[j] >= 0)
         for (int o = oa + threadIdx.x; o < ob; o += NT)
-          for (int u = 0; u < es.rs[j]; u += 32) prefetch_l2(pool.B + (static_cast<size_t>(es.ss[j]) * D + o) * R + u);
+          for (int u = 0; u < es.rs[j]; u += 32)
+            prefetch_l2(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[es.ss[j]] + u);
     ptx::grid_dependency_wait();
     ptx::grid_dependents_launch();
     *waited = true;
@@ -162,7 +163,7 @@ __device__ __forceinline__ void expand_vfull_token_item(float* __restrict__ y, c
     for (int j = 0; j < J; ++j) {
       const int s = es.ss[j];
       if (s < 0) continue;
-      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(s) * D + o) * R);
+      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[s]);
       float d = 0.f;
       for (int u = 0; u < (es.rs[j] + 7) / 8; ++u) d += ev_dot8(__ldg(brow + u), &es.vs[j][8 * u]);
       acc += d;

@@ -23,12 +23,16 @@
 //               stage back to both producers;
 //   warps 2..5  epilogue in each CTA: tcgen05.ld of its 128 rows (one per thread), stores to y,
 //               then an arrival on rank 0's accumulator-free barrier.
-// Extra K blocks (the fused expand of the tensor-core prefill path): the pair tile covers
-// M-tiles 2 mp and 2 mp + 1, whose slot lists may differ; the pair runs one 64-wide block per
-// slot in the union of both lists, in ascending slot order. Rank r's A operand is the scaled v
-// tile of its own M-tile for that slot, or zeros (an out-of-range TMA box) when its tile does
-// not use the slot; the B operand is the slot's B rows for the pair's output columns, split
-// between the ranks like W.
+// Extra K blocks (the expand of the LoRA side path, inside the accumulator): the pair tile covers
+// M-tiles 2 mp and 2 mp + 1, whose units (64-column blocks of the slot space used by their
+// tokens) may differ; the pair runs one block per entry of the union the metadata lists, in
+// ascending block order. Rank r's A operand is the scaled v tile of its own M-tile's unit on that
+// block, or zeros (an out-of-range TMA box) when its tile does not use the block; the B operand is
+// the block's 64 columns of B for the pair's output rows, split between the ranks like W.
+// Tile order: M fastest (the pairs working on one W column block run together, so W comes from
+// HBM once), with the rows of each column rotated by the column index, so that a row with many
+// extra blocks (decode tokens with many slots) is spread over all pairs instead of falling to the
+// same pairs in every wave.
 // Every wait is bounded (2 s); on a timeout a thread sets the error bit and leaves its loop.
 // Both CTAs always reach the final cluster barrier, so a timeout never turns into a hang.
 #include <cuda.h>
@@ -46,7 +50,6 @@ constexpr int kPairM = 2 * kHalf;
 constexpr int kPK = 64;                    // 64 bf16 = one 128-byte swizzle row
 constexpr int kPairThreads = 192;
 constexpr int kPairABytes = kHalf * kPK * 2;
-constexpr int kMaxPairExtra = 2 * kTileSlots;
 constexpr int kEpiBoxBytes = 32 * 32 * 4;    // y staging box: 32 rows x 32 fp32 columns
 
 // BN = columns of y per pair tile (W rows: BN / 2 per CTA); STAGES = ring depth that fits.
@@ -66,48 +69,25 @@ struct PairCfg {
   static_assert(kBytes <= 232448, "shared memory");
 };
 
-// Slots of the extra K blocks of pair tile mp: the ascending union of the slot lists of M-tiles
-// 2 mp and 2 mp + 1 (a tile past the end, or one with more than kTileSlots slots, contributes
-// none). With slot != nullptr it also fills slot[e] and own[e] = position of slot[e] in the list
-// of M-tile 2 mp + half (-1: that tile does not use the slot). Returns the count.
-__device__ __forceinline__ int pair_extra(const int32_t* tile_info, int mp, int num_m, int half, int* slot,
-                                          int* own) {
-  int c[2] = {0, 0};
-  const int32_t* l[2] = {nullptr, nullptr};
-  if (!tile_info) return 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int mb = 2 * mp + h;
-    if (mb < num_m) {
-      const int32_t* info = tile_info + mb * (kTileSlots + 1);
-      if (info[0] <= kTileSlots) {
-        c[h] = info[0];
-        l[h] = info + 1;
-      }
-    }
-  }
-  int i = 0, j = 0, n = 0;
-  while (i < c[0] || j < c[1]) {
-    const int a = i < c[0] ? l[0][i] : INT_MAX;
-    const int b = j < c[1] ? l[1][j] : INT_MAX;
-    const int s = a < b ? a : b;
-    if (slot) {
-      slot[n] = s;
-      own[n] = half == 0 ? (a == s ? i : -1) : (b == s ? j : -1);
-    }
-    if (a == s) ++i;
-    if (b == s) ++j;
-    ++n;
-  }
-  return n;
+// M row of the pair tile with sequence number `tile`: M fastest, rotated by the column index, which
+// keeps every column's rows a permutation while a persistent pair's tiles walk through the rows.
+__device__ __forceinline__ int pair_row(int tile, int num_mp) {
+  return (tile % num_mp + tile / num_mp) % num_mp;
+}
+
+// Extra K blocks of pair tile mp (0 without the fused side path).
+__device__ __forceinline__ int pair_extra(const int32_t* ptile_off, int mp) {
+  return ptile_off ? ptile_off[mp + 1] - ptile_off[mp] : 0;
 }
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kPairThreads, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_b,
-                      const __grid_constant__ CUtensorMap tmap_y, const int32_t* __restrict__ tile_info, int v_rows,
-                      float* __restrict__ y, int y_tma, int T, int D, int K, uint32_t* __restrict__ err) {
+                      const __grid_constant__ CUtensorMap tmap_y, const int32_t* __restrict__ ptile_off,
+                      const int32_t* __restrict__ pent_blk, const int32_t* __restrict__ pent_u0,
+                      const int32_t* __restrict__ pent_u1, int v_rows, float* __restrict__ y, int y_tma, int T, int D,
+                      int K, uint32_t* __restrict__ err) {
   using L = PairCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,15 +133,16 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      int slot[kMaxPairExtra], own[kMaxPairExtra];
+      const int32_t* own_unit = rank == 0 ? pent_u0 : pent_u1;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += n_pairs) {
-        const int mp = tile % num_mp;
+        const int mp = pair_row(tile, num_mp);
         const int m_blk = 2 * mp + static_cast<int>(rank);
         const int n0 = (tile / num_mp) * BN + static_cast<int>(rank) * L::kBRows;
-        const int n_extra = pair_extra(tile_info, mp, num_m, static_cast<int>(rank), slot, own);
+        const int n_extra = pair_extra(ptile_off, mp);
+        const int e0 = n_extra ? ptile_off[mp] : 0;
         for (int kb = 0; kb < num_kb + n_extra; ++kb) {
           if (!ptx::mbar_wait_short(&empty[stage], phase ^ 1u, err)) { ok = false; break; }
           uint8_t* sa = smem + stage * L::kStageBytes;
@@ -172,10 +153,11 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
             ptx::tma_load_2d_pair(sa, &tmap_x, bar, kb * kPK, m_blk * kHalf);
             ptx::tma_load_2d_pair(sb, &tmap_w, bar, kb * kPK, n0);
           } else {
-            const int i = kb - num_kb;
-            const int vrow = own[i] >= 0 ? (m_blk * kTileSlots + own[i]) * kHalf : v_rows;   // v_rows: zeros
+            const int e = e0 + kb - num_kb;
+            const int own = own_unit[e];
+            const int vrow = own >= 0 ? own * kHalf : v_rows;   // v_rows: past the end, zeros
             ptx::tma_load_2d_pair(sa, &tmap_v, bar, 0, vrow);
-            ptx::tma_load_2d_pair(sb, &tmap_b, bar, 0, slot[i] * D + n0);
+            ptx::tma_load_2d_pair(sb, &tmap_b, bar, pent_blk[e] * kBlockCols, n0);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -201,7 +183,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
         if (!ptx::mbar_wait_short(&acc_empty[acc], acc_phase ^ 1u, err)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * L::kAccStride);
-        const int n_kb = num_kb + pair_extra(tile_info, tile % num_mp, num_m, 0, nullptr, nullptr);
+        const int n_kb = num_kb + pair_extra(ptile_off, pair_row(tile, num_mp));
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!ptx::mbar_wait_short(&full[stage], phase, err)) { ok = false; break; }
           ptx::tc_fence_after();
@@ -229,7 +211,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
     int box = 0;
     int local = 0;
     for (int tile = pair; tile < num_tiles; tile += n_pairs, ++local) {
-      const int m0 = (2 * (tile % num_mp) + static_cast<int>(rank)) * kHalf;
+      const int m0 = (2 * pair_row(tile, num_mp) + static_cast<int>(rank)) * kHalf;
       const int n0 = (tile / num_mp) * BN;
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
@@ -310,14 +292,17 @@ cudaError_t launch_pair_bn(const uint16_t* x, const uint16_t* W, float* y, int T
   if (!make_tmap_bf16(&mx, x, T, K, kHalf, kPK) || !make_tmap_bf16(&mw, W, D, K, L::kBRows, kPK))
     return cudaErrorInvalidValue;
   const int num_m = (T + kHalf - 1) / kHalf;
-  const int32_t* tile_info = nullptr;
+  const int32_t *ptile_off = nullptr, *pent_blk = nullptr, *pent_u0 = nullptr, *pent_u1 = nullptr;
   int v_rows = 0;
-  if (pool && meta) {                     // the fused side path: v tiles and the pool's B rows
-    v_rows = num_m * kTileSlots * kHalf;
+  if (pool && meta) {                     // the fused side path: v tiles and the pool's B columns
+    v_rows = meta->unit_cap * kHalf;
     if (!make_tmap_bf16(&mv, meta->vtile, v_rows, kPK, kHalf, kPK) ||
-        !make_tmap_bf16(&mb, pool->B, static_cast<long>(pool->S) * D, pool->R, L::kBRows, kPK))
+        !make_tmap_bf16(&mb, pool->B, D, pool->C, L::kBRows, kPK))
       return cudaErrorInvalidValue;
-    tile_info = meta->tile_info;
+    ptile_off = meta->ptile_off;
+    pent_blk = meta->pent_blk;
+    pent_u0 = meta->pent_u0;
+    pent_u1 = meta->pent_u1;
   } else {
     mv = mx;
     mb = mw;
@@ -340,8 +325,8 @@ cudaError_t launch_pair_bn(const uint16_t* x, const uint16_t* W, float* y, int T
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   note_launch_begin(kKindGemm, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel<BN, STAGES>, mx, mw, mv, mb, my, tile_info, v_rows,
-                                     y, y_tma, T, D, K, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel<BN, STAGES>, mx, mw, mv, mb, my, ptile_off, pent_blk,
+                                     pent_u0, pent_u1, v_rows, y, y_tma, T, D, K, err);
   note_launch_end(kKindGemm, s);
   return e;
 }

@@ -42,21 +42,27 @@ struct GemmSmem {
   static constexpr int kBytes = kBarrierOffset + 256 + 1024;   // + barriers, + alignment slack
 };
 
-// Extra K blocks of the fused side path: for an M-tile whose tokens use at most kTileSlots slots,
-// one 64-wide block per slot with A operand = the scaled v tile (tensor-core shrink output) and
-// B operand = the slot's B rows of the N tile, both fetched by TMA into the same stage layout.
-__device__ __forceinline__ int extra_kblocks(const int32_t* tile_info, int m_blk) {
-  if (!tile_info) return 0;
-  const int c = tile_info[m_blk * (kTileSlots + 1)];
-  return c <= kTileSlots ? c : 0;
+// Extra K blocks of the fused side path: one per unit of the M-tile (a 64-column block of the slot
+// space used by its tokens) with A operand = the unit's scaled v tile (tensor-core shrink output)
+// and B operand = the block's 64 columns of B for the N tile, both fetched by TMA into the same
+// stage layout.
+__device__ __forceinline__ int extra_kblocks(const int32_t* tile_unit_off, int m_blk) {
+  return tile_unit_off ? tile_unit_off[m_blk + 1] - tile_unit_off[m_blk] : 0;
+}
+
+// M-tile of the tile with sequence number `tile`: M fastest, rotated by the column index (each
+// column's rows stay a permutation), so that M-tiles with many extra K blocks are spread over the
+// persistent CTAs.
+__device__ __forceinline__ int tc_row(int tile, int num_m) {
+  return (tile % num_m + tile / num_m) % num_m;
 }
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_b,
-                    const int32_t* __restrict__ tile_info, float* __restrict__ y, int T, int D, int K,
-                    uint32_t* __restrict__ err) {
+                    const int32_t* __restrict__ tile_unit_off, const int32_t* __restrict__ unit_blk,
+                    float* __restrict__ y, int T, int D, int K, uint32_t* __restrict__ err) {
   using L = GemmSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,10 +108,11 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile % num_m;
+        const int m_blk = tc_row(tile, num_m);
         const int m0 = m_blk * BM;
         const int n0 = (tile / num_m) * BN;
-        const int n_extra = extra_kblocks(tile_info, m_blk);
+        const int n_extra = extra_kblocks(tile_unit_off, m_blk);
+        const int u0 = n_extra ? tile_unit_off[m_blk] : 0;
         for (int kb = 0; kb < num_kb + n_extra; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) { ok = false; break; }
           uint8_t* sa = smem + stage * L::kStageBytes;
@@ -115,10 +122,9 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
             ptx::tma_load_2d(sa, &tmap_x, &full[stage], kb * BK, m0);
             ptx::tma_load_2d(sb, &tmap_w, &full[stage], kb * BK, n0);
           } else {
-            const int i = kb - num_kb;
-            const int slot = tile_info[m_blk * (kTileSlots + 1) + 1 + i];
-            ptx::tma_load_2d(sa, &tmap_v, &full[stage], 0, (m_blk * kTileSlots + i) * BM);
-            ptx::tma_load_2d(sb, &tmap_b, &full[stage], 0, slot * D + n0);
+            const int u = u0 + kb - num_kb;
+            ptx::tma_load_2d(sa, &tmap_v, &full[stage], 0, u * BM);
+            ptx::tma_load_2d(sb, &tmap_b, &full[stage], unit_blk[u] * kBlockCols, n0);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -137,7 +143,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
         if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, err)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const int n_kb = num_kb + extra_kblocks(tile_info, tile % num_m);
+        const int n_kb = num_kb + extra_kblocks(tile_unit_off, tc_row(tile, num_m));
         for (int kb = 0; kb < n_kb; ++kb) {
           if (!ptx::mbar_wait(&full[stage], phase, err)) { ok = false; break; }
           ptx::tc_fence_after();
@@ -163,7 +169,7 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
     const int row_in_tile = quarter * 32 + lane;
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      const int m0 = (tile % num_m) * BM;
+      const int m0 = tc_row(tile, num_m) * BM;
       const int n0 = (tile / num_m) * BN;
       const int acc = local & 1;
       const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
@@ -234,7 +240,6 @@ struct SkinnyShrink {
   int vfull_ld;
   int R;                     // rows per slot in the A pool (multiple of 8, divides 128)
   int n_ablk;                // A-row blocks in the grid (enough for every possible active slot)
-  int window;                // 1: shrink only, for the tokens of the step's overflow tiles (below)
 };
 
 // Tensor maps over the A pool with boxes of R, 2R, 4R, ... rows (up to 128): a run of 2^k active
@@ -317,14 +322,6 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   float* part = reinterpret_cast<float*>(smem);          // [NT][128] after the main loop
 
-  // window mode without a window this step: the metadata (built before the large-batch GEMM
-  // that precedes this kernel) says so, and the whole grid leaves at once, after the wait that
-  // keeps the launch order of later kernels
-  if (sh.window && sh.meta.counts[6] < 0) {
-    ptx::grid_dependency_wait();
-    ptx::grid_dependents_launch();
-    return;
-  }
   cg::cluster_group cluster = cg::this_cluster();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -370,7 +367,6 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
   if (a_blk) {
     n_act = *sh.n_act;
     idle = a0 >= n_act;                                 // uniform across the cluster
-    if (sh.window) idle = idle || sh.meta.counts[6] < 0;   // no window this step: nothing to do
     if (!idle && warp == 2) {                           // this block's adapter rows into L2
       const int n_box = min(spb, n_act - a0);
       for (int e = lane; e < n_box * (kb1 - kb0); e += 32) {
@@ -404,9 +400,6 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
         }
       }
       const uint32_t bytes = static_cast<uint32_t>(a_blk ? n_box * sh.R * BK * 2 + NT * BK * 2 : stage_bytes);
-      // window rows: tile counts[6] and, if present, tile counts[7] (else rows past x: zero fill)
-      const int win_row0 = sh.window ? sh.meta.counts[6] * BM : 0;
-      const int win_row1 = sh.window ? (sh.meta.counts[7] >= 0 ? sh.meta.counts[7] * BM : sh.meta.T + BM) : 0;
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -420,12 +413,7 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
         } else {
           ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
         }
-        if (sh.window) {                                // the window's two 128-token tiles (an absent
-          ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, win_row0);   // one reads
-          ptx::tma_load_2d(sa + kSkinnyABytes + BM * BK * 2, &tmap_x, &full[stage], kb * BK, win_row1);  // zeros)
-        } else {
-          ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
-        }
+        ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
         if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -552,13 +540,14 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
   CUtensorMap mx, mw, mv, mb;
   if (!make_tmap_bf16_impl(&mx, x, T, K, BM, BK) || !make_tmap_bf16_impl(&mw, W, D, K, BN, BK))
     return cudaErrorInvalidValue;
-  const int32_t* tile_info = nullptr;
-  if (pool && meta) {                     // the fused side path: v tiles and the pool's B rows
-    const long v_rows = static_cast<long>((T + BM - 1) / BM) * kTileSlots * BM;
+  const int32_t *tile_unit_off = nullptr, *unit_blk = nullptr;
+  if (pool && meta) {                     // the fused side path: v tiles and the pool's B columns
+    const long v_rows = static_cast<long>(meta->unit_cap) * BM;
     if (!make_tmap_bf16_impl(&mv, meta->vtile, v_rows, BK, BM, BK) ||
-        !make_tmap_bf16_impl(&mb, pool->B, static_cast<long>(pool->S) * D, pool->R, BN, BK))
+        !make_tmap_bf16_impl(&mb, pool->B, D, pool->C, BN, BK))
       return cudaErrorInvalidValue;
-    tile_info = meta->tile_info;
+    tile_unit_off = meta->tile_unit_off;
+    unit_blk = meta->unit_blk;
   } else {
     mv = mx;
     mb = mw;
@@ -566,7 +555,8 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
   const int tiles = ((T + BM - 1) / BM) * ((D + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   note_launch_begin(kKindGemm, s);
-  gemm_bf16_tc_kernel<BN, STAGES><<<grid, kGemmThreads, L::kBytes, s>>>(mx, mw, mv, mb, tile_info, y, T, D, K, err);
+  gemm_bf16_tc_kernel<BN, STAGES><<<grid, kGemmThreads, L::kBytes, s>>>(mx, mw, mv, mb, tile_unit_off, unit_blk, y, T,
+                                                                         D, K, err);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindGemm, s);
   return e;
@@ -583,8 +573,7 @@ int skinny_splitk(int n_oblk, int K, int num_sms) {
 
 cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                           int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
-  // window mode: the tokens are two 128-row tiles of x (256 rows of v), chosen on the device
-  const int NT = sh.window ? 2 * BM : (T + 15) / 16 * 16;
+  const int NT = (T + 15) / 16 * 16;
   const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
   const int splitk = skinny_splitk(n_oblk, K, num_sms);
   uint32_t tmem_cols = 32;
@@ -601,10 +590,7 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   }
   CUtensorMap mw, mx;
   SkinnyAMaps ma;
-  if (sh.window) {
-    if (!make_tmap_bf16_impl(&mx, x, T, K, BM, BK)) return cudaErrorInvalidValue;
-    mw = mx;                                            // no W blocks
-  } else if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) {
+  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) {
     return cudaErrorInvalidValue;
   }
   for (int k = 0; k < kABoxMaps; ++k) {
@@ -629,10 +615,10 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  note_launch_begin(sh.window ? kKindShrink : kKindGemm, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, sh.window ? NT : T, D, K, NT,
-                                     splitk, tmem_cols, err, sh);
-  note_launch_end(sh.window ? kKindShrink : kKindGemm, s);
+  note_launch_begin(kKindGemm, s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, T, D, K, NT, splitk, tmem_cols,
+                                     err, sh);
+  note_launch_end(kKindGemm, s);
   return e;
 }
 
@@ -702,22 +688,8 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
   const int max_act = std::min(pool.S, m.n);
   const int n_dchunk = (pool.D + kExpandVfullCols - 1) / kExpandVfullCols;
   SkinnyShrink sh{pool, m, n_dchunk, m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R,
-                  (max_act * pool.R + BM - 1) / BM, 0};
+                  (max_act * pool.R + BM - 1) / BM};
   return launch_skinny(x, W, y, m.T, pool.K, pool.D, err, num_sms, pool.A, pool.S, sh, s);
-}
-
-bool window_shrink_supported(int T, int J, int S, int R, int vfull_ld, int vfull_rows) {
-  if (T <= kSkinnyMaxT || vfull_rows < kSkinnyMaxT) return false;
-  if (R < 8 || R > BM || BM % R != 0) return false;
-  return std::min(S, T * J) * R <= vfull_ld;
-}
-
-cudaError_t launch_gemm_shrink_window(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
-                                      int num_sms, cudaStream_t s) {
-  const int max_act = std::min(pool.S, m.n);
-  SkinnyShrink sh{pool, m, 0, m.act_slot, m.counts + 4, m.vfull, m.vfull_ld, pool.R,
-                  (max_act * pool.R + BM - 1) / BM, 1};
-  return launch_skinny(x, nullptr, nullptr, m.T, pool.K, 0, err, num_sms, pool.A, pool.S, sh, s);
 }
 
 }  // namespace mlora

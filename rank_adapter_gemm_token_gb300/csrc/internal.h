@@ -15,15 +15,30 @@ constexpr int kPairBlock = 16;      // pairs of one slot handled together by the
 constexpr int kMetaThreads = 1024;
 constexpr int kMaxShrinkSplits = 16;   // K splits of the shrink (partial sums per split)
 constexpr int kMaxTiles = 512;         // 128-token M-tiles of a step (65535 tokens)
-constexpr int kTileSlots = 4;          // slots per M-tile handled on the tensor cores
+constexpr int kBlockCols = 64;         // columns of the slot space per extra K block (one 128-byte row)
+constexpr int kMaxTileUnits = 256;     // (M-tile, column block) units of one M-tile on the tensor cores
+constexpr int kMaxUnits = 16384;       // units of one step on the tensor cores (v tiles of 16 KB each)
+constexpr int kGroupUnits = 4;         // units of one M-tile shrunk together (MMA N = 64 per unit)
 
-// Device arrays of one adapter pool (one adapted linear).
+// Columns a slot of maximum rank r owns: 8, 16, 32 or 64, or a multiple of 64 above that, so that
+// with each class starting on a multiple of min(width, 64) no slot straddles two 64-column blocks.
+__host__ __device__ constexpr int slot_width(int r) {
+  return r <= 8 ? 8 : r <= 16 ? 16 : r <= 32 ? 32 : r <= 64 ? 64 : (r + 63) / 64 * 64;
+}
+
+// Device arrays of one adapter pool (one adapted linear). The slots' rank rows form one column
+// space of C columns: slot s owns columns off_s .. off_s + width_s - 1 (width = slot_width of its
+// class's maximum rank); A holds row c of that space for every column c, B holds column c.
 struct PoolView {
-  const uint16_t* A;        // [S, R, K] bf16, slot s row q at A + (s*R + q)*K
-  const uint16_t* B;        // [S, D, R] bf16, slot s row o at B + (s*D + o)*R
+  const uint16_t* A;        // [C, K] bf16: slot s row q at A + (off_s + q) * K
+  const uint16_t* B;        // [D, C] bf16: slot s row o at B + o * C + off_s
   const float* slot_scale;  // [S] alpha/r or alpha/sqrt(r)
   const int32_t* slot_rank; // [S] true rank, 0 = empty slot
-  int S, R, K, D;
+  const int32_t* slot_off;  // [S] first column of the slot
+  const int32_t* slot_width;// [S] columns of the slot
+  const int32_t* col_slot;  // [C] slot owning each column (-1: a gap between classes)
+  int S, R, C, K, D;        // R = the widest slot; with one rank class every slot is R wide (off_s = s R)
+  int uniform;              // 1: one rank class
 };
 
 // Device arrays of one step's metadata (see build_meta_kernel for the contents).
@@ -37,19 +52,32 @@ struct MetaView {
   int32_t* blk_start;   // [n]   start of the block inside order
   int32_t* blk_count;   // [n]   pairs in the block
   int32_t* counts;      // [8] n_seg, n_active, n_blocks, first rejected pair (INT32_MAX if none),
-                        //     n_act (distinct slots with an active pair), n_todo (entries of todo_blk)
+                        //     n_act (distinct slots with an active pair), n_todo (entries of todo_blk),
+                        //     n_units, n_groups (tensor-core side path, below)
   int32_t* pair_act;    // [n] index of the pair's slot among the active slots (-1: none)
   int32_t* act_slot;    // [n] active slots in ascending order
   uint32_t* err;        // device error word (ptx::kErr* bits)
   float* vpart;         // shrink output: [n_splits][n][R] fp32 partial sums of A x per K split
   float* vfull;         // small-batch shrink output: [T][act][R] fp32, row stride vfull_ld floats
   int vfull_ld;
-  int32_t* tile_info;   // per 128-token M-tile: [count, slot_0 .. slot_{kTileSlots-1}] (ascending,
-                        //   -1 unused); count > kTileSlots = too many slots (overflow tile)
-  int32_t* pair_fused;  // [n] 1: the pair's side path runs on the tensor cores inside the GEMM
-  int32_t* todo_blk;    // [n] ascending pair-block numbers holding a pair with pair_fused == 0
-  uint16_t* vtile;      // tensor-core shrink output: [tiles][kTileSlots][128][64] bf16, s c v per token
-  int n;                // pairs of the current step (T * J)
+  // Tensor-core side path. A unit is an (M-tile of 128 tokens, 64-column block of the slot space)
+  // with at least one active pair of the tile owning a column of the block; units are numbered
+  // tile by tile, blocks ascending. An M-tile with more than kMaxTileUnits units, or whose units do
+  // not fit in the unit capacity, overflows: its pairs take the CUDA-core kernels.
+  int32_t* tile_unit_off; // [tiles + 1] units of tile i: [tile_unit_off[i], tile_unit_off[i + 1])
+  int32_t* unit_blk;      // [U] column block of each unit
+  int32_t* unit_tile;     // [U] M-tile of each unit
+  int32_t* grp_unit;      // [U] shrink groups: first unit (kGroupUnits consecutive units of one tile)
+  int32_t* grp_cnt;       // [U] units in the group
+  int32_t* ptile_off;     // [pair tiles + 1] entries of pair tile mp (M-tiles 2mp, 2mp + 1)
+  int32_t* pent_blk;      // [U] column block of each pair-tile entry (ascending within a pair tile)
+  int32_t* pent_u0;       // [U] unit of M-tile 2mp with that block (-1: none)
+  int32_t* pent_u1;       // [U] unit of M-tile 2mp + 1 with that block (-1: none)
+  int32_t* pair_fused;    // [n] 1: the pair's side path runs on the tensor cores inside the GEMM
+  int32_t* todo_blk;      // [n] ascending pair-block numbers holding a pair with pair_fused == 0
+  uint16_t* vtile;        // [U][128][64] bf16: s c v of the unit's tokens on the block's columns
+  int unit_cap;           // U
+  int n;                  // pairs of the current step (T * J)
   int T, J;
 };
 
@@ -77,8 +105,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, long rows, int cols, int
 bool make_tmap_f32_sw128(CUtensorMap* map, const void* base, long rows, int cols, int box_rows);
 
 // Launchers. Each returns the cudaError_t of its launch.
-cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
-                              const int32_t* slot_rank, const MetaView& m, cudaStream_t s);
+// The step's metadata: sorted pairs, segments, pair-blocks, active slots and, for the tensor-core
+// side path, the units of each M-tile over the pool's column blocks.
+cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, const PoolView& pool,
+                              const MetaView& m, cudaStream_t s);
 
 // y[T, D] (fp32) = x[T, K] (bf16, row-major) * W[D, K]^T (bf16, row-major), tcgen05 path.
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
@@ -96,24 +126,12 @@ cudaError_t launch_gemm_shrink_fused(const uint16_t* x, const uint16_t* W, float
 cudaError_t launch_lora_expand_vfull(float* y, const PoolView& pool, const MetaView& m, int num_sms,
                                      cudaStream_t s);
 
-// Overflow window of a large batch (T > kSkinnyMaxT): when the step has one or two 128-token tiles
-// with more than kTileSlots slots (the metadata names them in counts[6], counts[7]; counts[6] is
-// -1 otherwise), their pairs take the small-batch machinery: the skinny kernel in shrink-only
-// mode over those 256 token rows (vfull row w = window row), then the vfull expand restricted to
-// the pairs not handled on the tensor cores. Both kernels do nothing when there is no window.
-bool window_shrink_supported(int T, int J, int S, int R, int vfull_ld, int vfull_rows);
-cudaError_t launch_gemm_shrink_window(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
-                                      int num_sms, cudaStream_t s);
-cudaError_t launch_lora_expand_window(float* y, const PoolView& pool, const MetaView& m, int num_sms,
-                                      cudaStream_t s);
-
-// Tensor-core prefill path (sgmv_tc.cu): pools with padded rank R == 64.
-bool sgmv_tc_supported(int R);
-// vtile = scaled (x A_slot^T) per (M-tile, slot) for tiles with at most kTileSlots slots.
-cudaError_t launch_sgmv_shrink_tc(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
+// Tensor-core shrink (shrink_tc.cu): vtile of every unit, i.e. for each (M-tile, column block)
+// the tile's x rows times the block's A rows, masked to each token's own slots and scaled.
+cudaError_t launch_lora_shrink_tc(const uint16_t* x, const PoolView& pool, const MetaView& m, uint32_t* err,
                                   int num_sms, cudaStream_t s);
-// Tiled base GEMM; with pool and meta it also adds vtile x B_slot^T as extra K blocks of the
-// fused tiles.
+// Tiled base GEMM; with pool and meta it also adds vtile x B^T as one extra K block per unit of
+// each M-tile (the expand inside the accumulator).
 cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                                   uint32_t* err, int num_sms, const PoolView* pool, const MetaView* meta,
                                   cudaStream_t s);
@@ -122,7 +140,7 @@ cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y
 cudaError_t launch_wait_check(uint32_t* err, cudaStream_t s);
 
 // CTA-pair (cta_group::2) tiled GEMM for large batches (gemm_pair.cu): 256 x 256 tiles of y on
-// clusters of two CTAs, with the same fused side-path K blocks as the one-CTA tiled GEMM.
+// clusters of two CTAs, with the side path's K blocks of both M-tiles of a pair tile.
 // pair_gemm_max_pairs() = clusters of two that can be resident at once (0: not available).
 // pair_gemm_pick_n() = the N tile (256, 224, 192 or 128) that best fills whole waves; bn = 0 in
 // launch_pair_gemm picks it. gemm_tile_n() is the process-wide choice set by
@@ -135,12 +153,10 @@ int gemm_tile_n();
 
 // K elements per shrink split and the number of splits for a pool of width R.
 void shrink_split(int K, int R, int* kc_len, int* n_ks);
-// CUDA-core shrink / expand; with skip_fused they leave out the pairs the tensor-core path handles,
-// and with window they also do nothing when the overflow-window kernels took the step's
-// remaining pairs (counts[6] >= 0).
+// CUDA-core shrink / expand; with skip_fused they leave out the pairs the tensor-core path handles.
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s, bool skip_fused = false, bool window = false);
+                               cudaStream_t s, bool skip_fused = false);
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
-                               bool skip_fused = false, bool window = false);
+                               bool skip_fused = false);
 
 }  // namespace mlora

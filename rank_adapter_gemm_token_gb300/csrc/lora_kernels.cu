@@ -66,8 +66,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
   constexpr int V = 8 / RPW;                                  // vectors per lane per row
   ptx::grid_dependents_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // skip_fused bit 1: the overflow-window kernels took the remaining pairs if there is a window
-  const int items = ((skip_fused & 2) && m.counts[6] >= 0) ? 0 : m.counts[skip_fused ? 5 : 2] * n_ks;
+  const int items = m.counts[skip_fused ? 5 : 2] * n_ks;
   const int K = pool.K, R = pool.R;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int bi = item / n_ks, ks = item - bi * n_ks;
@@ -76,6 +75,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
     const int start = m.blk_start[b];
     const int cnt = m.blk_count[b];
     const int rank = pool.slot_rank[slot];
+    const int aoff = pool.slot_off[slot];
     const int k0 = ks * kc_len;
     const int nv = (min(K, k0 + kc_len) - k0) / 8;            // vectors in this split
     for (int qg = warp; qg < rank; qg += 8 * RPW) {           // rows qg + 8 i, i < RPW
@@ -98,7 +98,7 @@ lora_shrink_kernel(const uint16_t* __restrict__ x, PoolView pool, MetaView m, in
 #pragma unroll
           for (int r = 0; r < RPW; ++r) {
             const int q = qg + 8 * r;
-            const uint4* arow = reinterpret_cast<const uint4*>(pool.A + (static_cast<size_t>(slot) * R + q) * K + k0);
+            const uint4* arow = reinterpret_cast<const uint4*>(pool.A + (static_cast<size_t>(aoff) + q) * K + k0);
 #pragma unroll
             for (int v = 0; v < V; ++v) {
               const int u = u0 + 32 * v;
@@ -153,8 +153,8 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
                            int skip_fused) {
   __shared__ __align__(16) float vs[kPairBlock][kMaxRank];
   __shared__ int tok[kPairBlock];
-  // skip_fused: only todo_blk's blocks; bit 1: nothing when the overflow-window kernels ran
-  const int items = ((skip_fused & 2) && m.counts[6] >= 0) ? 0 : m.counts[skip_fused ? 5 : 2] * n_dchunk;
+  // skip_fused: only todo_blk's blocks
+  const int items = m.counts[skip_fused ? 5 : 2] * n_dchunk;
   const int R = pool.R, D = pool.D;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int bi = item / n_dchunk, dc = item - bi * n_dchunk;
@@ -176,7 +176,7 @@ lora_expand_segment_kernel(float* __restrict__ y, PoolView pool, MetaView m, int
     __syncthreads();
     for (int o = dc * cols + threadIdx.x; o < min(D, (dc + 1) * cols);
          o += kExpandThreads) {
-      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(slot) * D + o) * R);
+      const uint4* brow = reinterpret_cast<const uint4*>(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[slot]);
       float d[kPairBlock];
 #pragma unroll
       for (int i = 0; i < kPairBlock; ++i) d[i] = 0.f;
@@ -202,7 +202,7 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
   __shared__ float cs[kMaxJ];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
   const int J = m.J, R = pool.R, D = pool.D;
-  const bool none = skip_fused && (m.counts[5] == 0 || ((skip_fused & 2) && m.counts[6] >= 0));
+  const bool none = skip_fused && m.counts[5] == 0;
   const int items = none ? 0 : m.T * n_dchunk;          // nothing left off the tensor cores
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int t = item / n_dchunk, dc = item - t * n_dchunk;
@@ -229,7 +229,7 @@ lora_expand_token_kernel(float* __restrict__ y, PoolView pool, MetaView m, int n
       for (int j = 0; j < J; ++j) {
         const int s = ss[j];
         if (s < 0) continue;
-        const uint4* brow = reinterpret_cast<const uint4*>(pool.B + (static_cast<size_t>(s) * D + o) * R);
+        const uint4* brow = reinterpret_cast<const uint4*>(pool.B + static_cast<size_t>(o) * pool.C + pool.slot_off[s]);
         float d = 0.f;
         for (int u = 0; u < (rs[j] + 7) / 8; ++u) d += dot8_bf16_f32(__ldg(brow + u), &vs[j][8 * u]);
         acc += d;
@@ -251,8 +251,8 @@ void shrink_split(int K, int R, int* kc_len, int* n_ks) {
 }
 
 cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const MetaView& m, int num_sms,
-                               cudaStream_t s, bool skip_fused, bool window) {
-  const int skip = skip_fused ? (window ? 3 : 1) : 0;
+                               cudaStream_t s, bool skip_fused) {
+  const int skip = skip_fused ? 1 : 0;
   if (m.n == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);
@@ -272,8 +272,8 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
 }
 
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
-                               bool skip_fused, bool window) {
-  const int skip = skip_fused ? (window ? 3 : 1) : 0;
+                               bool skip_fused) {
+  const int skip = skip_fused ? 1 : 0;
   if (m.n == 0 || pool.D == 0) return cudaSuccess;
   int kc, n_ks;
   shrink_split(pool.K, pool.R, &kc, &n_ks);

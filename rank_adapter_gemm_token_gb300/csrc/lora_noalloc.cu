@@ -10,6 +10,7 @@
 //
 // Two kernels: a gather shrink (one pair per block, whole K per adapter row, v written to the
 // workspace) and a token-major expand that adds a token's slots in order j = 0..J-1.
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -29,7 +30,8 @@ constexpr int kNoallocThreads = 256;
 constexpr int kNoallocCols = 512;          // output columns per expand block
 
 // Device address of g_noalloc_v per device ordinal. In host code the symbol's name is only a
-// host-side stand-in, so the address is looked up once per device with that device current.
+// host-side stand-in, so the address is looked up with that device current (on every call made
+// outside stream capture) and kept here for calls made inside one.
 float* g_noalloc_v_addr[64] = {};
 std::mutex g_noalloc_mu;
 
@@ -45,9 +47,13 @@ __device__ __forceinline__ float nd_dot8(const uint4& a, const uint4& b) {
   return s;
 }
 
-__device__ __forceinline__ int checked_slot(const int32_t* token_slots, const int32_t* slot_rank, int p, int S) {
+// A pair's slot if it names a slot in [0, S) whose rank is in [1, R], else -1 (adds nothing).
+__device__ __forceinline__ int checked_slot(const int32_t* token_slots, const int32_t* slot_rank, int p, int S,
+                                            int R) {
   const int s = token_slots[p];
-  return (s >= 0 && s < S && slot_rank[s] > 0) ? s : -1;   // anything else adds nothing
+  if (s < 0 || s >= S) return -1;
+  const int r = slot_rank[s];
+  return (r > 0 && r <= R) ? s : -1;
 }
 
 // One block per (token, slot) pair: warp w computes rows q = w, w + 8, ... of v = A_slot x_t over
@@ -58,7 +64,7 @@ noalloc_shrink_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict_
                       int K, int J, int n, float* __restrict__ v) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int p = blockIdx.x; p < n; p += gridDim.x) {
-    const int s = checked_slot(token_slots, slot_rank, p, S);
+    const int s = checked_slot(token_slots, slot_rank, p, S, R);
     if (s < 0) continue;
     const int rank = slot_rank[s];
     const uint4* xv = reinterpret_cast<const uint4*>(x + static_cast<size_t>(p / J) * K);
@@ -77,17 +83,17 @@ noalloc_shrink_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict_
 __global__ void __launch_bounds__(kNoallocThreads)
 noalloc_expand_kernel(float* __restrict__ y, const int32_t* __restrict__ token_slots, const float* __restrict__ scales,
                       const uint16_t* __restrict__ B_pool, const float* __restrict__ slot_scale,
-                      const int32_t* __restrict__ slot_rank, int S, int R, int D, int J, int T,
+                      const int32_t* __restrict__ slot_rank, int S, int R, int D, int J, int T, int n_dchunk,
                       const float* __restrict__ v) {
   __shared__ __align__(16) float vs[kMaxJ][kMaxRank];
   __shared__ int ss[kMaxJ], rs[kMaxJ];
-  const int n_dchunk = (D + kNoallocCols - 1) / kNoallocCols;
-  for (int item = blockIdx.x; item < T * n_dchunk; item += gridDim.x) {
+  const int items = T * n_dchunk;                       // checked to fit an int by the host
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int t = item / n_dchunk, dc = item - t * n_dchunk;
     __syncthreads();
     if (threadIdx.x < J) {
       const int p = t * J + threadIdx.x;
-      const int s = checked_slot(token_slots, slot_rank, p, S);
+      const int s = checked_slot(token_slots, slot_rank, p, S, R);
       ss[threadIdx.x] = s;
       rs[threadIdx.x] = s >= 0 ? slot_rank[s] : 0;
     }
@@ -160,14 +166,28 @@ extern "C" mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, 
              kNoallocVFloats);
     return report_error(MLORA_ERR_TOO_MANY_TOKENS, msg);
   }
+  const size_t n_dchunk = (static_cast<size_t>(D) + kNoallocCols - 1) / kNoallocCols;
+  if (static_cast<size_t>(T) * n_dchunk > static_cast<size_t>(INT_MAX))
+    return report_error(MLORA_ERR_INVALID_ARG, "T * ceil(D / 512) must fit in an int");
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return report_cuda_error(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return report_error(MLORA_ERR_INVALID_ARG, "device ordinal unsupported");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* v = nullptr;
   {
+    // outside a capture the address is looked up again (it changes when the device's context is
+    // re-created, e.g. after cudaDeviceReset); inside one the kept address is used
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+      cudaGetLastError();
+      cap = cudaStreamCaptureStatusActive;
+    }
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_v_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_noalloc_v_addr[dev]) {
+      if (cap != cudaStreamCaptureStatusNone)
+        return report_error(MLORA_ERR_INVALID_ARG,
+                            "the first call on a device must come before any stream capture (workspace address)");
       void* addr = nullptr;
       e = cudaGetSymbolAddress(&addr, g_noalloc_v);
       if (e != cudaSuccess) return report_cuda_error(e, "cudaGetSymbolAddress(workspace)");
@@ -178,7 +198,6 @@ extern "C" mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, 
   int num_sms = 0;
   e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return report_cuda_error(e, "SM count");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = T * J;
   int grid = n < num_sms * 8 ? n : num_sms * 8;
   note_launch_begin(kKindShrink, s);
@@ -187,11 +206,11 @@ extern "C" mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, 
   e = cudaGetLastError();
   note_launch_end(kKindShrink, s);
   if (e != cudaSuccess) return report_cuda_error(e, "shrink launch");
-  const int items = T * ((D + kNoallocCols - 1) / kNoallocCols);
+  const int items = T * static_cast<int>(n_dchunk);
   grid = items < num_sms * 8 ? items : num_sms * 8;
   note_launch_begin(kKindExpand, s);
   noalloc_expand_kernel<<<grid, kNoallocThreads, 0, s>>>(y, token_slots, scales, B_pool, slot_scale, slot_rank,
-                                                         n_slots, r_pad, D, J, T, v);
+                                                         n_slots, r_pad, D, J, T, static_cast<int>(n_dchunk), v);
   e = cudaGetLastError();
   note_launch_end(kKindExpand, s);
   if (e != cudaSuccess) return report_cuda_error(e, "expand launch");

@@ -22,8 +22,9 @@ namespace mlora {
 namespace {
 
 // Dynamic shared memory of the metadata kernel: the per-bin arrays (80 B per slot bin, up to
-// 164 KB at 2048 slots) plus, when they fit, four int arrays over the pairs (16 B per pair).
-// The kernel's static arrays (~11 KB) come on top, within the 227 KB a block may use.
+// 164 KB at 2048 slots; later reused for two column-block bitmaps per warp) plus, when they fit,
+// four int arrays over the pairs (16 B per pair). The kernel's static arrays (~10 KB) come on
+// top, within the 227 KB a block may use.
 constexpr size_t kMetaMaxDynSmem = 200 * 1024;
 
 __device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& pa, int& pb, int& pc,
@@ -56,19 +57,58 @@ __device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& 
   __syncthreads();
 }
 
+// Exclusive prefix of per-lane counts over the warp; returns the exclusive prefix and sets *total.
+__device__ __forceinline__ int warp_exclusive(int c, int* total) {
+  const int lane = threadIdx.x & 31;
+  int inc = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += t;
+  }
+  *total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - c;
+}
+
+// Bitmap (n_words words) of the column blocks owned by the slots of M-tile `tile`'s active pairs;
+// one warp. A slot of width w at column offset off covers blocks off / 64 .. (off + w - 1) / 64.
+__device__ __forceinline__ void tile_block_bitmap(uint32_t* bm, int n_words, int tile, int T, int J,
+                                                  const int* pslot, const int32_t* slot_off,
+                                                  const int32_t* slot_width) {
+  const int lane = threadIdx.x & 31;
+  for (int k = lane; k < n_words; k += 32) bm[k] = 0u;
+  __syncwarp();
+  const int p0 = tile * 128 * J, p1 = min(T, tile * 128 + 128) * J;
+  for (int p = p0 + lane; p < p1; p += 32) {
+    const int s = pslot[p];
+    if (s < 0) continue;
+    const int off = slot_off[s];
+    const int b1 = (off + slot_width[s] - 1) / kBlockCols;
+    for (int b = off / kBlockCols; b <= b1; ++b) atomicOr(&bm[b >> 5], 1u << (b & 31));
+  }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kMetaThreads, 1)
-build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, int S,
-                  const int32_t* __restrict__ slot_rank, MetaView m, int cache) {
+build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, PoolView pool,
+                  MetaView m, int cache) {
   extern __shared__ int smem[];
+  const int S = pool.S;
   const int nb = S + 1;
   int* hist = smem;                          // [nb] pairs per bin
   int* cursor = hist + nb;                   // [nb] next free position of each bin
   int* chunk_tot = cursor + nb;              // [nb] pairs per bin in the current chunk
   int* actidx = chunk_tot + nb;              // [nb] index among the active slots (-1: none)
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
+  const int n_blocks = (pool.C + kBlockCols - 1) / kBlockCols;  // column blocks of the slot space
+  const int n_words = (n_blocks + 31) / 32;
+  // after the sort the bins' area holds two block bitmaps per warp (the host sized it for both)
+  uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem);
+  const size_t bins_bytes = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
+  const size_t bm_bytes = static_cast<size_t>(32) * 2 * n_words * sizeof(uint32_t);
   // small steps keep their pair slots, order and pair-blocks in shared memory as well, so the
   // later steps read them there instead of going back to global memory
-  int* c_base = reinterpret_cast<int*>(wcnt + 32 * nb);
+  int* c_base = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(smem) + ((bins_bytes > bm_bytes ? bins_bytes : bm_bytes) + 15) / 16 * 16);
   int* pslot = cache ? c_base : m.pair_slot;            // [n] validated slot per pair
   int* ord = cache ? c_base + n : m.order;              // [n] sorted pair order
   int* bstart = cache ? c_base + 2 * n : m.blk_start;   // [n] pair-block starts
@@ -76,12 +116,14 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __shared__ int warp_sums[96];
   __shared__ int first_bad;
   __shared__ int n_blk_sh;                               // pair-blocks in total
-  __shared__ int ovf_n, ovf_a, ovf_b;                    // overflow tiles: count, first two
-  __shared__ int tile_cnt[kMaxTiles];                    // distinct slots per 128-token M-tile
-  __shared__ int tile_list[kMaxTiles * kTileSlots];
+  __shared__ int tile_cnt[kMaxTiles];                    // units per 128-token M-tile (0 if it overflows)
+  __shared__ int tile_off[kMaxTiles + 1];                // first unit of each M-tile
+  __shared__ int tile_grp[kMaxTiles];                    // first shrink group of each M-tile
+  __shared__ uint8_t tile_ovf[kMaxTiles];                // 1: the tile's pairs take the CUDA-core kernels
+  __shared__ int ptile_cnt[kMaxTiles / 2];               // entries per pair tile
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  ptx::grid_dependents_launch();             // the first linear's GEMM may start its set-up
+  ptx::grid_dependents_launch();             // the first linear's kernels may start their set-up
   // the first chunk's inputs are loaded while the slot table is staged
   const int s_first = tid < n ? token_slots[tid] : -1;
   const float c_first = tid < n && scales ? scales[tid] : 1.0f;
@@ -89,7 +131,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   //    `cursor` is free until step 2
   for (int b = tid; b < nb; b += kMetaThreads) {
     hist[b] = 0;
-    if (b < S) cursor[b] = slot_rank[b] > 0;
+    if (b < S) cursor[b] = pool.slot_rank[b] > 0;
   }
   if (tid == 0) first_bad = INT_MAX;
   __syncthreads();
@@ -193,80 +235,136 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     __syncthreads();
   }
 
-  // Steps 4 and 5 serve only the tensor-core prefill path, which batches of at most
-  // kSkinnyMaxT tokens never take (they use the small-batch path or the CUDA-core kernels).
-  if (m.T <= kSkinnyMaxT) {
-    if (tid == 0) {
-      m.counts[3] = first_bad;
-      m.counts[5] = 0;
-      m.counts[6] = -1;
-      m.counts[7] = -1;
-      if (first_bad != INT_MAX) atomicOr(m.err, ptx::kErrBadSlot);
-    }
-    return;
-  }
-
-  // 4. slots of each 128-token M-tile (x order), for the tensor-core prefill path: within a
-  //    segment the pairs are in token order, so the first pair of each (slot, tile) run adds the
-  //    slot to that tile's list; a tile with more than kTileSlots slots overflows.
+  // 4. units of the tensor-core side path: for each 128-token M-tile the column blocks its active
+  //    pairs' slots own (warp per tile, bitmap over the blocks), counted, capped, numbered.
   const int n_tiles = (m.T + 127) / 128;
-  for (int i = tid; i < n_tiles; i += kMetaThreads) tile_cnt[i] = 0;
+  const int n_ptiles = (n_tiles + 1) / 2;
+  uint32_t* bmA = bitmaps + warp * 2 * n_words;
+  uint32_t* bmB = bmA + n_words;
+  for (int i = warp; i < n_tiles; i += 32) {
+    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    int c = 0;
+    for (int w = lane; w < n_words; w += 32) c += __popc(bmA[w]);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    if (lane == 0) tile_cnt[i] = c;
+    __syncwarp();
+  }
   __syncthreads();
-  for (int i = tid; i < n; i += kMetaThreads) {
-    const int p = ord[i];
-    const int s = pslot[p];
-    if (s < 0) continue;
-    const int tile = (p / m.J) >> 7;
-    bool first = true;
-    if (i > 0) {
-      const int q = ord[i - 1];
-      first = pslot[q] != s || ((q / m.J) >> 7) != tile;
+  {
+    // a tile with too many units, or whose units would pass the capacity, overflows (every later
+    // tile with units then overflows as well, since the units are numbered in tile order)
+    const int c = tid < n_tiles ? tile_cnt[tid] : 0;
+    const int capped = c <= kMaxTileUnits ? c : 0;
+    int off, unused0, unused1;
+    block_exclusive_scan3(capped, 0, 0, off, unused0, unused1, warp_sums);
+    const bool ovf = c > kMaxTileUnits || off + capped > m.unit_cap;
+    const int fin = ovf ? 0 : c;
+    int uoff, goff;
+    block_exclusive_scan3(fin, (fin + kGroupUnits - 1) / kGroupUnits, 0, uoff, goff, unused1, warp_sums);
+    if (tid < n_tiles) {
+      tile_cnt[tid] = fin;
+      tile_off[tid] = uoff;
+      tile_grp[tid] = goff;
+      tile_ovf[tid] = ovf ? 1 : 0;
+      m.tile_unit_off[tid] = uoff;
     }
-    if (first) {
-      const int k = atomicAdd(&tile_cnt[tile], 1);
-      if (k < kTileSlots) tile_list[tile * kTileSlots + k] = s;
+    if (tid == n_tiles - 1) {
+      tile_off[n_tiles] = uoff + fin;
+      m.tile_unit_off[n_tiles] = uoff + fin;
+      m.counts[6] = uoff + fin;
+      m.counts[7] = goff + (fin + kGroupUnits - 1) / kGroupUnits;
+    }
+    if (n_tiles == 0 && tid == 0) {
+      m.tile_unit_off[0] = 0;
+      m.counts[6] = 0;
+      m.counts[7] = 0;
     }
   }
   __syncthreads();
-  for (int tile = tid; tile < n_tiles; tile += kMetaThreads) {   // ascending slot order per tile
-    const int c = tile_cnt[tile];
-    int* l = &tile_list[tile * kTileSlots];
-    const int k = c < kTileSlots ? c : kTileSlots;
-    for (int a = 1; a < k; ++a)
-      for (int b = a; b > 0 && l[b - 1] > l[b]; --b) {
-        const int t = l[b];
-        l[b] = l[b - 1];
-        l[b - 1] = t;
+  // units in ascending block order per tile, and the shrink's groups of consecutive units
+  for (int i = warp; i < n_tiles; i += 32) {
+    const int cnt = tile_cnt[i];
+    if (cnt == 0) continue;
+    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    const int ubase = tile_off[i];
+    int run = 0;
+    for (int k0 = 0; k0 < n_words; k0 += 32) {
+      const int kw = k0 + lane;
+      uint32_t w = kw < n_words ? bmA[kw] : 0u;
+      int total;
+      int pos = run + warp_exclusive(__popc(w), &total);
+      while (w) {
+        const int bit = __ffs(w) - 1;
+        w &= w - 1u;
+        m.unit_blk[ubase + pos] = kw * 32 + bit;
+        m.unit_tile[ubase + pos] = i;
+        ++pos;
       }
-    m.tile_info[tile * (kTileSlots + 1)] = c;
-    for (int a = 0; a < kTileSlots; ++a) m.tile_info[tile * (kTileSlots + 1) + 1 + a] = a < k ? l[a] : -1;
-  }
-  __syncthreads();
-  for (int p = tid; p < n; p += kMetaThreads)
-    m.pair_fused[p] = pslot[p] >= 0 && tile_cnt[(p / m.J) >> 7] <= kTileSlots;
-
-  // the overflow window: with one or two overflow tiles, counts[6] and counts[7] name them in
-  // ascending order (counts[7] = -1 for one); otherwise both are -1 (none, or too many)
-  if (tid == 0) {
-    ovf_n = 0;
-    ovf_a = INT_MAX;
-    ovf_b = INT_MAX;
-  }
-  __syncthreads();
-  for (int tile = tid; tile < n_tiles; tile += kMetaThreads)
-    if (tile_cnt[tile] > kTileSlots) {
-      atomicAdd(&ovf_n, 1);
-      atomicMin(&ovf_a, tile);
+      run += total;
     }
-  __syncthreads();
-  for (int tile = tid; tile < n_tiles; tile += kMetaThreads)
-    if (tile_cnt[tile] > kTileSlots && tile != ovf_a) atomicMin(&ovf_b, tile);
-  __syncthreads();
-  if (tid == 0) {
-    const bool win = ovf_n == 1 || ovf_n == 2;
-    m.counts[6] = win ? ovf_a : -1;
-    m.counts[7] = win && ovf_n == 2 ? ovf_b : -1;
+    for (int g = lane; g * kGroupUnits < cnt; g += 32) {
+      m.grp_unit[tile_grp[i] + g] = ubase + g * kGroupUnits;
+      m.grp_cnt[tile_grp[i] + g] = min(kGroupUnits, cnt - g * kGroupUnits);
+    }
   }
+  // pair tiles (M-tiles 2 mp and 2 mp + 1): the union of both tiles' blocks, each entry with the
+  // unit of either tile on that block (-1 where the tile does not use it)
+  for (int mp = warp; mp < n_ptiles; mp += 32) {
+    const int ta = 2 * mp, tb = 2 * mp + 1;
+    const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
+    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    int c = 0;
+    for (int w = lane; w < n_words; w += 32) c += __popc((ha ? bmA[w] : 0u) | (hb ? bmB[w] : 0u));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    if (lane == 0) ptile_cnt[mp] = c;
+    __syncwarp();
+  }
+  __syncthreads();
+  {
+    const int c = tid < n_ptiles ? ptile_cnt[tid] : 0;
+    int off, unused0, unused1;
+    block_exclusive_scan3(c, 0, 0, off, unused0, unused1, warp_sums);
+    if (tid < n_ptiles) m.ptile_off[tid] = off;
+    if (tid == n_ptiles - 1) m.ptile_off[n_ptiles] = off + c;
+    if (n_ptiles == 0 && tid == 0) m.ptile_off[0] = 0;
+    if (tid < n_ptiles) ptile_cnt[tid] = off;          // from here: first entry of the pair tile
+  }
+  __syncthreads();
+  for (int mp = warp; mp < n_ptiles; mp += 32) {
+    const int ta = 2 * mp, tb = 2 * mp + 1;
+    const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
+    if (!ha && !hb) continue;
+    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    int ra = 0, rb = 0, ru = 0;
+    const int ua = tile_off[ta], ub = hb ? tile_off[tb] : 0, ebase = ptile_cnt[mp];
+    for (int k0 = 0; k0 < n_words; k0 += 32) {
+      const int kw = k0 + lane;
+      const uint32_t wa = (ha && kw < n_words) ? bmA[kw] : 0u, wb = (hb && kw < n_words) ? bmB[kw] : 0u;
+      uint32_t wu = wa | wb;
+      int ta_tot, tb_tot, tu_tot;
+      const int pa = ra + warp_exclusive(__popc(wa), &ta_tot);
+      const int pb = rb + warp_exclusive(__popc(wb), &tb_tot);
+      const int pu = ru + warp_exclusive(__popc(wu), &tu_tot);
+      const uint32_t all = wu;
+      while (wu) {
+        const int bit = __ffs(wu) - 1;
+        wu &= wu - 1u;
+        const uint32_t below = (1u << bit) - 1u;
+        const int e = ebase + pu + __popc(all & below);
+        m.pent_blk[e] = kw * 32 + bit;
+        m.pent_u0[e] = (wa >> bit) & 1u ? ua + pa + __popc(wa & below) : -1;
+        m.pent_u1[e] = (wb >> bit) & 1u ? ub + pb + __popc(wb & below) : -1;
+      }
+      ra += ta_tot;
+      rb += tb_tot;
+      ru += tu_tot;
+    }
+  }
+  for (int p = tid; p < n; p += kMetaThreads) m.pair_fused[p] = pslot[p] >= 0 && !tile_ovf[(p / m.J) >> 7];
 
   // 5. the pair-blocks that still need the CUDA-core shrink/expand (a pair in an overflow tile),
   //    in ascending order, so those kernels skip the fused blocks without looking at them
@@ -274,7 +372,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     auto todo = [&](int b) {
       const int start = bstart[b], cnt = bcount[b];
       bool t = false;
-      for (int i = 0; i < cnt; ++i) t |= tile_cnt[(ord[start + i] / m.J) >> 7] > kTileSlots;
+      for (int i = 0; i < cnt; ++i) t |= tile_ovf[(ord[start + i] / m.J) >> 7] != 0;
       return t;
     };
     const int nblk = n_blk_sh;
@@ -297,22 +395,28 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
 
 }  // namespace
 
-cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, int S,
-                              const int32_t* slot_rank, const MetaView& m, cudaStream_t s) {
-  const int nb = S + 1;
+cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, const PoolView& pool,
+                              const MetaView& m, cudaStream_t s) {
+  const int nb = pool.S + 1;
   const int n = T * J;
   const size_t bins = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
-  const int cache = bins + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
-  const size_t smem = bins + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);
-  static bool configured = false;
-  if (!configured) {
+  const size_t n_words = (static_cast<size_t>(pool.C) + kBlockCols * 32 - 1) / (kBlockCols * 32);
+  const size_t bitmaps = 32 * 2 * n_words * sizeof(uint32_t);
+  const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16;
+  if (front > kMetaMaxDynSmem) return cudaErrorInvalidValue;
+  const int cache = front + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
+  const size_t smem = front + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(build_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMetaMaxDynSmem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured_device = dev;
   }
   note_launch_begin(kKindMeta, s);
-  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, S, slot_rank, m, cache);
+  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, pool, m, cache);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindMeta, s);
   return e;

@@ -51,6 +51,7 @@ mlora_status cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_gemm_tile_n{0};          // mlora_set_gemm_tile_n
+std::atomic<int> g_path{0};                 // mlora_set_path
 
 // ---------------------------------------------------------------- trace
 struct TraceRec {
@@ -92,7 +93,6 @@ mlora_status device_state(DeviceState** out) {
   return MLORA_OK;
 }
 
-int pad8(int r) { return (r + 7) / 8 * 8; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -138,11 +138,17 @@ void note_launch_end(int kind, cudaStream_t s) {
 struct mlora_pool {
   int device = 0;
   int S = 0, r_max = 0, R = 0, K = 0, D = 0;
-  uint16_t* A = nullptr;
-  uint16_t* B = nullptr;
+  int C = 0;                                   // columns of the slot space
+  uint16_t* A = nullptr;                       // [C, K]
+  uint16_t* B = nullptr;                       // [D, C]
   float* slot_scale = nullptr;
   int32_t* slot_rank = nullptr;
-  std::vector<int> h_rank;
+  int32_t* slot_off = nullptr;                 // [S] first column of each slot
+  int32_t* slot_width = nullptr;               // [S] columns of each slot
+  int32_t* col_slot = nullptr;                 // [C] slot owning each column
+  std::vector<int> class_slots, class_rank;    // the rank classes (one for mlora_pool_create)
+  std::vector<int> h_rank, h_off, h_width, h_class;
+  int max_span = 1;                            // most 64-column blocks one slot touches
   cudaStream_t copy_stream = nullptr;
   bool own_stream = false;
   cudaEvent_t load_done = nullptr, use_done = nullptr;
@@ -155,7 +161,10 @@ struct mlora_pool {
   std::vector<std::pair<cudaStream_t, uint64_t>> users;
   std::mutex mu;
 
-  PoolView view() const { return PoolView{A, B, slot_scale, slot_rank, S, R, K, D}; }
+  bool uniform() const { return class_slots.size() == 1; }
+  PoolView view() const {
+    return PoolView{A, B, slot_scale, slot_rank, slot_off, slot_width, col_slot, S, R, C, K, D, uniform() ? 1 : 0};
+  }
 };
 
 struct mlora_meta {
@@ -169,17 +178,51 @@ struct mlora_meta {
   float* vpart = nullptr;
   float* vfull = nullptr;
   int vfull_ld = 0;
-  int32_t *tile_info = nullptr, *pair_fused = nullptr, *todo_blk = nullptr;
+  int32_t *tile_unit_off = nullptr, *unit_blk = nullptr, *unit_tile = nullptr, *grp_unit = nullptr,
+          *grp_cnt = nullptr, *ptile_off = nullptr, *pent_blk = nullptr, *pent_u0 = nullptr, *pent_u1 = nullptr,
+          *pair_fused = nullptr, *todo_blk = nullptr;
   uint16_t* vtile = nullptr;
+  int unit_cap = 0;
   int T = 0, J = 1, S = -1;
+  std::vector<int> class_slots, class_rank;    // layout of the pool the last build used
   bool built = false;
   cudaEvent_t done = nullptr;
   cudaStream_t last_stream = nullptr;          // the stream of the last call that used the metadata
 
   MetaView view() const {
-    return MetaView{order, seg_slot, seg_off, pair_slot, pair_scale, blk_slot, blk_start, blk_count, counts,
-                    pair_act, act_slot, err, vpart, vfull, vfull_ld, tile_info, pair_fused, todo_blk, vtile,
-                    T * J, T, J};
+    MetaView v{};
+    v.order = order;
+    v.seg_slot = seg_slot;
+    v.seg_off = seg_off;
+    v.pair_slot = pair_slot;
+    v.pair_scale = pair_scale;
+    v.blk_slot = blk_slot;
+    v.blk_start = blk_start;
+    v.blk_count = blk_count;
+    v.counts = counts;
+    v.pair_act = pair_act;
+    v.act_slot = act_slot;
+    v.err = err;
+    v.vpart = vpart;
+    v.vfull = vfull;
+    v.vfull_ld = vfull_ld;
+    v.tile_unit_off = tile_unit_off;
+    v.unit_blk = unit_blk;
+    v.unit_tile = unit_tile;
+    v.grp_unit = grp_unit;
+    v.grp_cnt = grp_cnt;
+    v.ptile_off = ptile_off;
+    v.pent_blk = pent_blk;
+    v.pent_u0 = pent_u0;
+    v.pent_u1 = pent_u1;
+    v.pair_fused = pair_fused;
+    v.todo_blk = todo_blk;
+    v.vtile = vtile;
+    v.unit_cap = unit_cap;
+    v.n = T * J;
+    v.T = T;
+    v.J = J;
+    return v;
   }
 };
 
@@ -204,6 +247,12 @@ mlora_status mlora_set_gemm_tile_n(int n) {
   if (n != 0 && n != -1 && n != 256 && n != 224 && n != 192 && n != 128)
     return fail(MLORA_ERR_INVALID_ARG, "tile N must be 0 (automatic), -1 (one-CTA kernel), 256, 224, 192 or 128");
   g_gemm_tile_n.store(n);
+  return MLORA_OK;
+}
+
+mlora_status mlora_set_path(int path) {
+  if (path < 0 || path > 2) return fail(MLORA_ERR_INVALID_ARG, "path must be 0 (automatic), 1 or 2");
+  g_path.store(path);
   return MLORA_OK;
 }
 
@@ -236,18 +285,32 @@ const char* mlora_kernel_kind_name(int kind) {
 
 size_t mlora_pool_bytes(int n_slots, int r_max, int K, int D) {
   if (n_slots < 1 || r_max < 1 || K < 1 || D < 1) return 0;
-  return static_cast<size_t>(n_slots) * static_cast<size_t>(pad8(r_max)) *
+  return static_cast<size_t>(n_slots) * static_cast<size_t>(slot_width(r_max)) *
          (static_cast<size_t>(K) + static_cast<size_t>(D)) * 2u;
 }
 
 // ---------------------------------------------------------------- pool
-mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_stream, mlora_pool_t* out) {
+// Slots are numbered class by class; slot i of class c owns the next width_c = slot_width(rank_c)
+// columns of the slot space (each class starting on a multiple of min(width_c, 64), so no slot
+// straddles two 64-column blocks), so a pool's layout is a function of its class list alone and
+// pools created with the same classes lay out their slots identically.
+static mlora_status pool_create(int n_classes, const int* class_slots, const int* class_rank, int K, int D,
+                                void* copy_stream, mlora_pool_t* out) {
   if (!out) return fail(MLORA_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (n_slots < 1 || n_slots > MLORA_MAX_SLOTS)
-    return fail(MLORA_ERR_INVALID_ARG, "n_slots %d outside [1, %d]", n_slots, MLORA_MAX_SLOTS);
-  if (r_max < 1 || r_max > MLORA_MAX_RANK)
-    return fail(MLORA_ERR_INVALID_ARG, "r_max %d outside [1, %d]", r_max, MLORA_MAX_RANK);
+  if (n_classes < 1 || n_classes > MLORA_MAX_CLASSES || !class_slots || !class_rank)
+    return fail(MLORA_ERR_INVALID_ARG, "n_classes %d outside [1, %d] or a class array is NULL", n_classes,
+                MLORA_MAX_CLASSES);
+  long S = 0;
+  int r_max = 0;
+  for (int c = 0; c < n_classes; ++c) {
+    if (class_slots[c] < 1) return fail(MLORA_ERR_INVALID_ARG, "class %d has %d slots", c, class_slots[c]);
+    if (class_rank[c] < 1 || class_rank[c] > MLORA_MAX_RANK)
+      return fail(MLORA_ERR_INVALID_ARG, "class %d: rank %d outside [1, %d]", c, class_rank[c], MLORA_MAX_RANK);
+    S += class_slots[c];
+    r_max = std::max(r_max, class_rank[c]);
+  }
+  if (S > MLORA_MAX_SLOTS) return fail(MLORA_ERR_INVALID_ARG, "%ld slots: more than %d", S, MLORA_MAX_SLOTS);
   if (K < 8 || K % 8 != 0) return fail(MLORA_ERR_INVALID_ARG, "K %d must be a positive multiple of 8", K);
   if (D < 1) return fail(MLORA_ERR_INVALID_ARG, "D %d must be positive", D);
   DeviceState* ds = nullptr;
@@ -255,28 +318,54 @@ mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_
   mlora_pool* p = new (std::nothrow) mlora_pool();
   if (!p) return fail(MLORA_ERR_OOM, "host allocation failed");
   cudaGetDevice(&p->device);
-  p->S = n_slots;
+  p->S = static_cast<int>(S);
   p->r_max = r_max;
-  p->R = pad8(r_max);
+  p->R = slot_width(r_max);
   p->K = K;
   p->D = D;
-  p->h_rank.assign(n_slots, 0);
-  const size_t a_bytes = static_cast<size_t>(n_slots) * p->R * K * 2;
-  const size_t b_bytes = static_cast<size_t>(n_slots) * D * p->R * 2;
+  p->class_slots.assign(class_slots, class_slots + n_classes);
+  p->class_rank.assign(class_rank, class_rank + n_classes);
+  p->h_rank.assign(p->S, 0);
+  int col = 0;
+  for (int c = 0; c < n_classes; ++c) {
+    const int w = slot_width(class_rank[c]);
+    const int align = std::min(w, kBlockCols);
+    col = (col + align - 1) / align * align;
+    for (int i = 0; i < class_slots[c]; ++i) {
+      p->h_off.push_back(col);
+      p->h_width.push_back(w);
+      p->h_class.push_back(c);
+      p->max_span = std::max(p->max_span, (col + w - 1) / kBlockCols - col / kBlockCols + 1);
+      col += w;
+    }
+  }
+  p->C = col;
+  std::vector<int32_t> col_slot(p->C, -1);
+  for (int sl = 0; sl < p->S; ++sl)
+    for (int q = 0; q < p->h_width[sl]; ++q) col_slot[p->h_off[sl] + q] = sl;
+  const size_t a_bytes = static_cast<size_t>(p->C) * K * 2;
+  const size_t b_bytes = static_cast<size_t>(D) * p->C * 2;
   cudaError_t e = cudaSuccess;
   if ((e = cudaMalloc(&p->A, a_bytes)) != cudaSuccess || (e = cudaMalloc(&p->B, b_bytes)) != cudaSuccess ||
-      (e = cudaMalloc(&p->slot_scale, n_slots * sizeof(float))) != cudaSuccess ||
-      (e = cudaMalloc(&p->slot_rank, n_slots * sizeof(int32_t))) != cudaSuccess) {
+      (e = cudaMalloc(&p->slot_scale, p->S * sizeof(float))) != cudaSuccess ||
+      (e = cudaMalloc(&p->slot_rank, p->S * sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMalloc(&p->slot_off, p->S * sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMalloc(&p->slot_width, p->S * sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMalloc(&p->col_slot, p->C * sizeof(int32_t))) != cudaSuccess) {
     cudaGetLastError();
     mlora_pool_destroy(p);
     return e == cudaErrorMemoryAllocation ? fail(MLORA_ERR_OOM, "cudaMalloc of %zu + %zu bytes failed", a_bytes, b_bytes)
                                           : cuda_fail(e, "cudaMalloc");
   }
   if ((e = cudaMemset(p->A, 0, a_bytes)) != cudaSuccess || (e = cudaMemset(p->B, 0, b_bytes)) != cudaSuccess ||
-      (e = cudaMemset(p->slot_scale, 0, n_slots * sizeof(float))) != cudaSuccess ||
-      (e = cudaMemset(p->slot_rank, 0, n_slots * sizeof(int32_t))) != cudaSuccess) {
+      (e = cudaMemset(p->slot_scale, 0, p->S * sizeof(float))) != cudaSuccess ||
+      (e = cudaMemset(p->slot_rank, 0, p->S * sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMemcpy(p->slot_off, p->h_off.data(), p->S * sizeof(int32_t), cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMemcpy(p->slot_width, p->h_width.data(), p->S * sizeof(int32_t), cudaMemcpyHostToDevice)) !=
+          cudaSuccess ||
+      (e = cudaMemcpy(p->col_slot, col_slot.data(), p->C * sizeof(int32_t), cudaMemcpyHostToDevice)) != cudaSuccess) {
     mlora_pool_destroy(p);
-    return cuda_fail(e, "cudaMemset(pool)");
+    return cuda_fail(e, "pool initialisation");
   }
   if (copy_stream) {
     p->copy_stream = static_cast<cudaStream_t>(copy_stream);
@@ -300,6 +389,30 @@ mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_
   return MLORA_OK;
 }
 
+mlora_status mlora_pool_create(int n_slots, int r_max, int K, int D, void* copy_stream, mlora_pool_t* out) {
+  if (out) *out = nullptr;
+  if (n_slots < 1 || n_slots > MLORA_MAX_SLOTS)
+    return fail(MLORA_ERR_INVALID_ARG, "n_slots %d outside [1, %d]", n_slots, MLORA_MAX_SLOTS);
+  if (r_max < 1 || r_max > MLORA_MAX_RANK)
+    return fail(MLORA_ERR_INVALID_ARG, "r_max %d outside [1, %d]", r_max, MLORA_MAX_RANK);
+  return pool_create(1, &n_slots, &r_max, K, D, copy_stream, out);
+}
+
+mlora_status mlora_pool_create_classes(int n_classes, const int* class_slots, const int* class_rank, int K, int D,
+                                       void* copy_stream, mlora_pool_t* out) {
+  return pool_create(n_classes, class_slots, class_rank, K, D, copy_stream, out);
+}
+
+mlora_status mlora_pool_layout(mlora_pool_t p, int* C, int32_t* slot_off, int32_t* slot_width) {
+  if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+  if (C) *C = p->C;
+  for (int sl = 0; sl < p->S; ++sl) {
+    if (slot_off) slot_off[sl] = p->h_off[sl];
+    if (slot_width) slot_width[sl] = p->h_width[sl];
+  }
+  return MLORA_OK;
+}
+
 mlora_status mlora_pool_destroy(mlora_pool_t p) {
   if (!p) return MLORA_OK;
   if (p->has_load) cudaEventSynchronize(p->load_done);
@@ -312,14 +425,18 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
   cudaFree(p->B);
   cudaFree(p->slot_scale);
   cudaFree(p->slot_rank);
+  cudaFree(p->slot_off);
+  cudaFree(p->slot_width);
+  cudaFree(p->col_slot);
   delete p;
   return MLORA_OK;
 }
 
 // Writes a slot on the pool's copy stream after every call already queued on the pool: zeroes
-// it, then copies n_slices adapters of rank r each; slice i's A [r, K] goes to rows i r .. and its
-// B [widths[i], r] to rows off_i .. (off_i = sum of the earlier widths) and columns i r .. of the
-// slot's B (block-diagonal; a plain adapter is one slice of width D). n_slices = 0 clears it.
+// its columns (rows off .. off + width - 1 of A, columns off .. of B), then copies n_slices
+// adapters of rank r each; slice i's A [r, K] goes to rows off + i r .. and its B [widths[i], r]
+// to rows o_i .. (o_i = sum of the earlier widths) and columns off + i r .. of B (block-diagonal; a
+// plain adapter is one slice of width D). n_slices = 0 clears it.
 static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, const int* widths,
                                       const mlora_bf16* const* A_host, const mlora_bf16* const* B_host, int r,
                                       float alpha, int rslora) {
@@ -328,21 +445,24 @@ static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, co
     MLORA_CUDA(cudaEventRecord(p->use_done, u.first), "record use event");
     MLORA_CUDA(cudaStreamWaitEvent(cs, p->use_done, 0), "wait for last use of the pool");
   }
-  uint16_t* a_slot = p->A + static_cast<size_t>(slot) * p->R * p->K;
-  uint16_t* b_slot = p->B + static_cast<size_t>(slot) * p->D * p->R;
-  MLORA_CUDA(cudaMemsetAsync(a_slot, 0, static_cast<size_t>(p->R) * p->K * 2, cs), "zero slot A");
-  MLORA_CUDA(cudaMemsetAsync(b_slot, 0, static_cast<size_t>(p->D) * p->R * 2, cs), "zero slot B");
-  int off = 0;
+  const size_t off = static_cast<size_t>(p->h_off[slot]);
+  const size_t width = static_cast<size_t>(p->h_width[slot]);
+  const size_t pitch = static_cast<size_t>(p->C) * 2;
+  uint16_t* a_slot = p->A + off * p->K;
+  uint16_t* b_slot = p->B + off;
+  MLORA_CUDA(cudaMemsetAsync(a_slot, 0, width * p->K * 2, cs), "zero slot A");
+  MLORA_CUDA(cudaMemset2DAsync(b_slot, pitch, 0, width * 2, static_cast<size_t>(p->D), cs), "zero slot B");
+  int row = 0;
   for (int i = 0; i < n_slices; ++i) {
     const int w = widths ? widths[i] : p->D;
     MLORA_CUDA(cudaMemcpyAsync(a_slot + static_cast<size_t>(i) * r * p->K, A_host[i], static_cast<size_t>(r) * p->K * 2,
                                cudaMemcpyHostToDevice, cs),
                "copy A into slot");
-    MLORA_CUDA(cudaMemcpy2DAsync(b_slot + static_cast<size_t>(off) * p->R + static_cast<size_t>(i) * r,
-                                 static_cast<size_t>(p->R) * 2, B_host[i], static_cast<size_t>(r) * 2,
-                                 static_cast<size_t>(r) * 2, static_cast<size_t>(w), cudaMemcpyHostToDevice, cs),
+    MLORA_CUDA(cudaMemcpy2DAsync(b_slot + static_cast<size_t>(row) * p->C + static_cast<size_t>(i) * r, pitch, B_host[i],
+                                 static_cast<size_t>(r) * 2, static_cast<size_t>(r) * 2, static_cast<size_t>(w),
+                                 cudaMemcpyHostToDevice, cs),
                "copy B into slot");
-    off += w;
+    row += w;
   }
   const int rank = n_slices * r;
   note_launch_begin(kKindSlot, cs);
@@ -357,14 +477,21 @@ static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, co
   return MLORA_OK;
 }
 
+// The largest rank slot `slot` accepts (its class's rank).
+static int slot_rank_limit(mlora_pool_t p, int slot) { return p->class_rank[p->h_class[slot]]; }
+
 mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const mlora_bf16* A_host, const mlora_bf16* B_host,
                                 int rank, float alpha, int rslora) {
   if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
   if (slot < 0 || slot >= p->S) return fail(MLORA_ERR_SLOT_RANGE, "slot %d outside [0, %d)", slot, p->S);
   if (rank < 1 || !std::isfinite(alpha))
     return fail(MLORA_ERR_RANK_INVALID, "rank %d must be >= 1 and alpha finite", rank);
-  if (rank > p->r_max)
-    return fail(MLORA_ERR_RANK_TOO_LARGE, "adapter rank %d is larger than the pool's max rank %d", rank, p->r_max);
+  if (rank > slot_rank_limit(p, slot)) {
+    if (p->uniform())
+      return fail(MLORA_ERR_RANK_TOO_LARGE, "adapter rank %d is larger than the pool's max rank %d", rank, p->r_max);
+    return fail(MLORA_ERR_RANK_TOO_LARGE, "adapter rank %d is larger than the max rank %d of slot %d's class", rank,
+                slot_rank_limit(p, slot), slot);
+  }
   if (!A_host || !B_host) return fail(MLORA_ERR_INVALID_ARG, "A_host or B_host is NULL");
   std::lock_guard<std::mutex> lk(p->mu);
   int dev = 0;
@@ -390,9 +517,9 @@ mlora_status mlora_load_adapter_sliced(mlora_pool_t p, int slot, int n_slices, c
   if (total != p->D) return fail(MLORA_ERR_INVALID_ARG, "slice widths add up to %ld, the pool's D is %d", total, p->D);
   if (rank < 1 || !std::isfinite(alpha))
     return fail(MLORA_ERR_RANK_INVALID, "rank %d must be >= 1 and alpha finite", rank);
-  if (static_cast<long>(n_slices) * rank > p->r_max)
-    return fail(MLORA_ERR_RANK_TOO_LARGE, "%d slices of rank %d need rank %d, larger than the pool's max rank %d",
-                n_slices, rank, n_slices * rank, p->r_max);
+  if (static_cast<long>(n_slices) * rank > slot_rank_limit(p, slot))
+    return fail(MLORA_ERR_RANK_TOO_LARGE, "%d slices of rank %d need rank %d, larger than slot %d's max rank %d",
+                n_slices, rank, n_slices * rank, slot, slot_rank_limit(p, slot));
   std::lock_guard<std::mutex> lk(p->mu);
   int dev = 0;
   cudaGetDevice(&dev);
@@ -463,7 +590,7 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   m->max_tokens = max_tokens;
   m->J_max = J_max;
   m->r_max = r_max;
-  m->R_max = pad8(r_max);
+  m->R_max = slot_width(r_max);
   m->n_max = max_tokens * J_max;
   const size_t n = static_cast<size_t>(m->n_max);
   cudaError_t e = cudaSuccess;
@@ -483,12 +610,24 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->act_slot), (n + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->err), 4);
   alloc(reinterpret_cast<void**>(&m->vpart), static_cast<size_t>(kMaxShrinkSplits) * n * m->R_max * 4);
-  // tensor-core prefill path: per-tile slot lists, fused-pair flags, scaled v tiles (bf16)
+  // tensor-core side path: units (M-tile, 64-column block), their shrink groups, the pair tiles'
+  // entry lists and one bf16 v tile [128][64] per unit
   const size_t n_tiles = (static_cast<size_t>(max_tokens) + 127) / 128;
-  alloc(reinterpret_cast<void**>(&m->tile_info), n_tiles * (kTileSlots + 1) * 4);
+  const size_t span = static_cast<size_t>((m->R_max + kBlockCols - 1) / kBlockCols);   // blocks per slot
+  m->unit_cap = static_cast<int>(std::min(std::min(n * span, n_tiles * kMaxTileUnits), static_cast<size_t>(kMaxUnits)));
+  const size_t U = static_cast<size_t>(m->unit_cap);
+  alloc(reinterpret_cast<void**>(&m->tile_unit_off), (n_tiles + 1) * 4);
+  alloc(reinterpret_cast<void**>(&m->unit_blk), U * 4);
+  alloc(reinterpret_cast<void**>(&m->unit_tile), U * 4);
+  alloc(reinterpret_cast<void**>(&m->grp_unit), U * 4);
+  alloc(reinterpret_cast<void**>(&m->grp_cnt), U * 4);
+  alloc(reinterpret_cast<void**>(&m->ptile_off), ((n_tiles + 1) / 2 + 1) * 4);
+  alloc(reinterpret_cast<void**>(&m->pent_blk), U * 4);
+  alloc(reinterpret_cast<void**>(&m->pent_u0), U * 4);
+  alloc(reinterpret_cast<void**>(&m->pent_u1), U * 4);
   alloc(reinterpret_cast<void**>(&m->pair_fused), n * 4);
   alloc(reinterpret_cast<void**>(&m->todo_blk), n * 4);
-  alloc(reinterpret_cast<void**>(&m->vtile), n_tiles * kTileSlots * 128 * 64 * 2);
+  alloc(reinterpret_cast<void**>(&m->vtile), U * 128 * kBlockCols * 2);
   // small-batch shrink output: v of every token (up to 256) against every active slot
   const int vt = std::min(max_tokens, kVfullMaxTokens);
   m->vfull_ld = std::min(m->n_max, kVfullMaxAct) * m->R_max;
@@ -527,7 +666,15 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->vfull);
   cudaFree(m->pair_act);
   cudaFree(m->act_slot);
-  cudaFree(m->tile_info);
+  cudaFree(m->tile_unit_off);
+  cudaFree(m->unit_blk);
+  cudaFree(m->unit_tile);
+  cudaFree(m->grp_unit);
+  cudaFree(m->grp_cnt);
+  cudaFree(m->ptile_off);
+  cudaFree(m->pent_blk);
+  cudaFree(m->pent_u0);
+  cudaFree(m->pent_u1);
   cudaFree(m->pair_fused);
   cudaFree(m->todo_blk);
   cudaFree(m->vtile);
@@ -550,8 +697,10 @@ mlora_status mlora_build_meta(mlora_meta_t m, const int32_t* token_slots, const 
   m->T = T;
   m->J = J;
   m->S = pool->S;
+  m->class_slots = pool->class_slots;
+  m->class_rank = pool->class_rank;
   MetaView v = m->view();
-  cudaError_t e = launch_build_meta(token_slots, scales, T, J, pool->S, pool->slot_rank, v, s);
+  cudaError_t e = launch_build_meta(token_slots, scales, T, J, pool->view(), v, s);
   if (e != cudaSuccess) return cuda_fail(e, "build_meta launch");
   m->last_stream = s;
   m->built = true;
@@ -634,6 +783,8 @@ static mlora_status check_pair(mlora_pool_t p, mlora_meta_t m) {
   if (!m->built) return fail(MLORA_ERR_INVALID_ARG, "metadata has not been built");
   if (m->S != p->S)
     return fail(MLORA_ERR_MISMATCH, "metadata was built for %d slots, pool has %d", m->S, p->S);
+  if (m->class_slots != p->class_slots || m->class_rank != p->class_rank)
+    return fail(MLORA_ERR_MISMATCH, "metadata was built on a pool with other rank classes");
   if (p->R > m->R_max) return fail(MLORA_ERR_MISMATCH, "pool rank width %d exceeds the metadata's %d", p->R, m->R_max);
   return MLORA_OK;
 }
@@ -675,40 +826,41 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
   const MetaView mv = m->view();
   const PoolView pv = p->view();
   cudaError_t e = cudaSuccess;
-  if (skinny_shrink_fusable(m->T, m->J, p->S, p->R, m->vfull_ld) && (p->D + 127) / 128 <= ds->num_sms) {
+  if (m->T == 0) {
+    m->last_stream = s;
+    return MLORA_OK;
+  }
+  const int path = g_path.load(std::memory_order_relaxed);
+  const bool small_ok = p->uniform() && skinny_shrink_fusable(m->T, m->J, p->S, p->R, m->vfull_ld) &&
+                        (p->D + 127) / 128 <= ds->num_sms;
+  // the small-batch kernel multiplies every token by every active slot's rows: worth it while
+  // those rows add at most half of the output's 128-row blocks
+  const long act_blocks = (static_cast<long>(std::min(p->S, m->T * m->J)) * p->R + 127) / 128;
+  const bool small = small_ok && (path == 1 || (path == 0 && 2 * act_blocks <= (p->D + 127) / 128));
+  if (small) {
     // small batch whose 128-column output blocks fit in one wave: one split-K tensor-core kernel
     // for the base product and the shrink of every active slot, then the expand as its
-    // programmatic dependent (wider outputs, an LM head for instance, take the tiled GEMM and the
-    // separate shrink and expand below)
+    // programmatic dependent
     if ((e = launch_gemm_shrink_fused(x, W, y, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "fused GEMM launch");
     if ((e = launch_lora_expand_vfull(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
-  } else if (m->T > kSkinnyMaxT && sgmv_tc_supported(p->R)) {
-    // larger batch, rank width 64: tiles whose tokens use few slots get the shrink on the tensor
-    // cores and the expand as extra K blocks of the base GEMM; the rest take the CUDA-core path
-    if ((e = launch_sgmv_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "SGMV shrink launch");
+  } else {
+    // tensor-core side path: the shrink of every unit (M-tile, column block), then the base GEMM
+    // with the expand as extra K blocks; the CUDA-core kernels take the pairs of M-tiles that
+    // overflow the unit lists, and are launched only when the sizes allow an overflow
+    if ((e = launch_lora_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "tensor-core shrink launch");
     if ((e = launch_base_gemm_lora(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, &pv, &mv, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");
-    // one or two overflow tiles (decode-like tokens of a mixed batch): the small-batch shrink and
-    // expand over those tokens; more overflow tiles: the CUDA-core kernels (each kind does
-    // nothing when the other one applies)
-    const bool win = window_shrink_supported(m->T, m->J, p->S, p->R, m->vfull_ld,
-                                             std::min(m->max_tokens, kVfullMaxTokens));
-    if (win) {
-      if ((e = launch_gemm_shrink_window(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
-        return cuda_fail(e, "window shrink launch");
-      if ((e = launch_lora_expand_window(y, pv, mv, ds->num_sms, s)) != cudaSuccess)
-        return cuda_fail(e, "window expand launch");
+    const long n_blocks = (p->C + kBlockCols - 1) / kBlockCols;
+    const long per_tile = std::min(128L * m->J * p->max_span, n_blocks);
+    const long n_tiles = (m->T + 127) / 128;
+    const bool overflow = per_tile > kMaxTileUnits ||
+                          (n_tiles * per_tile > m->unit_cap && static_cast<long>(m->T) * m->J * p->max_span > m->unit_cap);
+    if (overflow) {
+      if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "shrink launch");
+      if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "expand launch");
     }
-    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s, true, win)) != cudaSuccess)
-      return cuda_fail(e, "shrink launch");
-    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true, win)) != cudaSuccess)
-      return cuda_fail(e, "expand launch");
-  } else {
-    if ((e = launch_base_gemm(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, s)) != cudaSuccess)
-      return cuda_fail(e, "base GEMM launch");
-    if ((e = launch_lora_shrink(x, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "shrink launch");
-    if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s)) != cudaSuccess) return cuda_fail(e, "expand launch");
   }
   m->last_stream = s;
   return MLORA_OK;

@@ -28,11 +28,22 @@ def _pinned_bits(a) -> torch.Tensor:
 
 
 class AdapterPool:
-    """Stacked slots A [S, R, K], B [S, D, R] (bf16, zero padded) of one adapted linear."""
+    """The slots of one adapted linear: A [C, K] and B [D, C] (bf16, zero padded) over a column
+    space in which slot s owns its rank rows. With `classes` = [(n_slots_c, rank_c), ...] the slots
+    come in rank classes (numbered class by class); otherwise n_slots slots of rank r_max."""
 
-    def __init__(self, n_slots: int, r_max: int, K: int, D: int, copy_stream=None):
-        self.n_slots, self.r_max, self.K, self.D = n_slots, r_max, K, D
-        self.handle = mlora.mlora_pool_create(n_slots, r_max, K, D, copy_stream)
+    def __init__(self, n_slots: int, r_max: int, K: int, D: int, copy_stream=None, classes=None):
+        self.K, self.D = K, D
+        if classes:
+            self.classes = [(int(n), int(r)) for n, r in classes]
+            self.n_slots = sum(n for n, _ in self.classes)
+            self.r_max = max(r for _, r in self.classes)
+            self.handle = mlora.mlora_pool_create_classes([n for n, _ in self.classes], [r for _, r in self.classes],
+                                                          K, D, copy_stream)
+        else:
+            self.classes = None
+            self.n_slots, self.r_max = n_slots, r_max
+            self.handle = mlora.mlora_pool_create(n_slots, r_max, K, D, copy_stream)
         self._staged = []           # pinned host copies kept alive until the next sync
 
     def load(self, slot: int, A, B, rank: int, alpha: float, rslora: bool = False) -> None:
@@ -50,6 +61,9 @@ class AdapterPool:
 
     def info(self) -> dict:
         return mlora.mlora_pool_info(self.handle)
+
+    def layout(self) -> dict:
+        return mlora.mlora_pool_layout(self.handle, self.n_slots)
 
     def close(self) -> None:
         if self.handle:

@@ -39,7 +39,8 @@ EXPORTS = (
     "mlora_load_adapter_sliced", "mlora_slot_cache_create", "mlora_slot_cache_destroy", "mlora_slot_cache_assign",
     "mlora_slot_cache_lookup", "mlora_slot_cache_pin", "mlora_slot_cache_evict", "mlora_adapter_cache_create",
     "mlora_adapter_cache_destroy", "mlora_adapter_cache_register", "mlora_adapter_cache_unregister",
-    "mlora_adapter_cache_pin", "mlora_adapter_cache_map",
+    "mlora_adapter_cache_pin", "mlora_adapter_cache_map", "mlora_pool_create_classes", "mlora_pool_layout",
+    "mlora_set_path",
 )
 
 
@@ -70,6 +71,9 @@ def load(path: str | None = None):
         vp, i32, f32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
         sig = {
             "mlora_pool_create": [i32, i32, i32, i32, vp, vp],
+            "mlora_pool_create_classes": [i32, vp, vp, i32, i32, vp, vp],
+            "mlora_pool_layout": [vp, vp, vp, vp],
+            "mlora_set_path": [i32],
             "mlora_pool_destroy": [vp],
             "mlora_load_adapter": [vp, i32, vp, vp, i32, f32, i32],
             "mlora_clear_slot": [vp, i32],
@@ -152,6 +156,28 @@ def mlora_pool_create(n_slots: int, r_max: int, K: int, D: int, copy_stream=None
     out = ctypes.c_void_p()
     _check(lib.mlora_pool_create(n_slots, r_max, K, D, _stream(copy_stream), ctypes.byref(out)), "mlora_pool_create")
     return out.value
+
+
+def mlora_pool_create_classes(class_slots, class_rank, K: int, D: int, copy_stream=None) -> int:
+    """A pool whose slots come in rank classes: class c has class_slots[c] slots of rank <= class_rank[c]."""
+    lib = load()
+    n = len(class_slots)
+    assert len(class_rank) == n
+    cs = (ctypes.c_int * n)(*[int(v) for v in class_slots])
+    cr = (ctypes.c_int * n)(*[int(v) for v in class_rank])
+    out = ctypes.c_void_p()
+    _check(lib.mlora_pool_create_classes(n, cs, cr, K, D, _stream(copy_stream), ctypes.byref(out)),
+           "mlora_pool_create_classes")
+    return out.value
+
+
+def mlora_pool_layout(pool: int, n_slots: int) -> dict:
+    """The pool's column space: C and each slot's first column and width."""
+    c = ctypes.c_int()
+    off = (ctypes.c_int32 * n_slots)()
+    width = (ctypes.c_int32 * n_slots)()
+    _check(load().mlora_pool_layout(pool, ctypes.byref(c), off, width), "mlora_pool_layout")
+    return dict(C=c.value, slot_off=list(off), slot_width=list(width))
 
 
 def mlora_pool_destroy(pool: int) -> None:
@@ -258,6 +284,11 @@ def mlora_lora_apply_noalloc(x, y, token_slots, scales, T: int, J: int, A_pool, 
     _check(load().mlora_lora_apply_noalloc(_ptr(x), _ptr(y), _ptr(token_slots), _ptr(scales), T, J, _ptr(A_pool),
                                            _ptr(B_pool), _ptr(slot_scale), _ptr(slot_rank), n_slots, r_pad, K, D,
                                            _stream(stream)), "mlora_lora_apply_noalloc")
+
+
+def mlora_set_path(path: int) -> None:
+    """0 automatic, 1 the small-batch path whenever allowed, 2 always the tensor-core side path."""
+    _check(load().mlora_set_path(path), "mlora_set_path")
 
 
 def mlora_set_gemm_tile_n(n: int) -> None:

@@ -154,6 +154,8 @@ class Workload:
     xs: dict                        # x_id -> [T, K] bf16 bits
     linears: list
     notes: str = ""
+    phases: list = field(default_factory=list)   # (name, first token, end token) sub-batches
+    classes: list | None = None     # [(slots, rank), ...] rank classes of the pools (None: one class)
 
 
 def _adapter(seed, layer, module, adapter_id, K, D, rank, alpha, rslora, std=0.02):
@@ -282,13 +284,15 @@ def logits(T: int = 256, hidden: int = 4096, vocab: int = 128256, n_adapters: in
 
 
 def zipf_admission(n_requests: int, n_ids: int, exponent: float, max_distinct: int,
-                   seed: int, tid: int) -> list:
+                   seed: int, tid: int, class_of=None, class_cap=None) -> list:
     """Draw request tenants from Zipf(exponent) over ids 1..n_ids and admit them in order: a
     request whose adapter is new is deferred when the batch already holds max_distinct adapters
-    (the max-loras admission rule). Returns the admitted tenant ids in admission order."""
+    (the max-loras admission rule) or, with class_of / class_cap, when the adapter's rank class
+    already holds class_cap[class_of(id)] adapters. Returns the admitted ids in admission order."""
     w = 1.0 / np.arange(1, n_ids + 1, dtype=np.float64) ** exponent
     cdf = np.cumsum(w) / w.sum()
     admitted, distinct, i = [], [], 0
+    per_class = {}
     u = uniform01(seed, tid, 64 * n_requests + 64)
     while len(admitted) < n_requests and i < len(u):
         a = int(np.searchsorted(cdf, u[i], side="right")) + 1
@@ -296,30 +300,65 @@ def zipf_admission(n_requests: int, n_ids: int, exponent: float, max_distinct: i
         if a not in distinct:
             if len(distinct) >= max_distinct:
                 continue
+            if class_cap is not None:
+                c = class_of(a)
+                if per_class.get(c, 0) >= class_cap[c]:
+                    continue
+                per_class[c] = per_class.get(c, 0) + 1
             distinct.append(a)
         admitted.append(a)
     return admitted
 
 
+MIXED_RANKS = (8, 16, 64)
+
+
+def mixed_class_slots(n_slots: int = 128, n_registered: int = 1000) -> list:
+    """Slots per rank class of the mixed step's pools: n_slots split in proportion to the
+    registered adapters of each rank (rank of id a = MIXED_RANKS[a mod 3]), largest remainder."""
+    counts = [sum(1 for a in range(1, n_registered + 1) if a % 3 == c) for c in range(3)]
+    quota = [n_slots * c / n_registered for c in counts]
+    out = [int(q) for q in quota]
+    for c in sorted(range(3), key=lambda c: (-(quota[c] - out[c]), c))[:n_slots - sum(out)]:
+        out[c] += 1
+    return out
+
+
 def mixed_step_plan(n_prefill: int = 4, prefill_len: int = 192, n_decode: int = 256,
                     n_registered: int = 1000, n_slots: int = 128, zipf: float = 1.1,
-                    seed_offset: int = 5):
+                    seed_offset: int = 5, classes: bool = True):
     """Mixed serving step: 4 prefill segments of 192 tokens (one request each) then 256 decode
-    tokens (one request each); tenants Zipf(1.1) over 1000 registered ids; admitted adapters
-    map to slots 0..n-1 in first-seen order; rank by id is [8, 16, 64][id mod 3], alpha = 2r."""
+    tokens (one request each); tenants Zipf(1.1) over 1000 registered ids; rank by id is
+    [8, 16, 64][id mod 3], alpha = 2r. With classes (default) the 128 slots form three rank
+    classes (8, 16, 64) sized by mixed_class_slots, a new adapter is admitted only while its
+    class has a free slot, and class c's adapters take its slots in first-seen order (slots are
+    numbered class by class); without, any adapter takes the next of 128 slots of rank 64."""
     seed = SEED_BASE + seed_offset
+    class_of = lambda a: a % 3  # noqa: E731
+    sizes = mixed_class_slots(n_slots, n_registered) if classes else None
     tenants = zipf_admission(n_prefill + n_decode, n_registered, zipf, n_slots, seed,
-                             tensor_key(_NS_MISC, 0))
+                             tensor_key(_NS_MISC, 0), class_of=class_of if classes else None, class_cap=sizes)
     slot_of = {}
-    for a in tenants:
-        slot_of.setdefault(a, len(slot_of))
+    if classes:
+        base = [0, sizes[0], sizes[0] + sizes[1]]
+        used = [0, 0, 0]
+        for a in tenants:
+            if a not in slot_of:
+                c = class_of(a)
+                slot_of[a] = base[c] + used[c]
+                used[c] += 1
+    else:
+        for a in tenants:
+            slot_of.setdefault(a, len(slot_of))
     per_token = []
     for i, a in enumerate(tenants):
         per_token += [slot_of[a]] * (prefill_len if i < n_prefill else 1)
     T = len(per_token)
-    ranks = {a: (8, 16, 64)[a % 3] for a in slot_of}
+    ranks = {a: MIXED_RANKS[a % 3] for a in slot_of}
     return dict(seed=seed, T=T, token_slots=np.array(per_token, dtype=np.int32).reshape(T, 1),
-                slot_of=slot_of, rank_of=ranks, tenants=tenants)
+                slot_of=slot_of, rank_of=ranks, tenants=tenants,
+                classes=[(sizes[c], MIXED_RANKS[c]) for c in range(3)] if classes else None,
+                n_prefill_tokens=n_prefill * prefill_len)
 
 
 MIXED_MODULES = (("qkv", 4096, 6144, 0), ("o", 4096, 4096, 1),
@@ -327,7 +366,7 @@ MIXED_MODULES = (("qkv", 4096, 6144, 0), ("o", 4096, 4096, 1),
 
 
 def mixed_adapter(seed: int, layer: int, module: int, adapter_id: int, K: int, D: int) -> Adapter:
-    r = (8, 16, 64)[adapter_id % 3]
+    r = MIXED_RANKS[adapter_id % 3]
     return _adapter(seed, layer, module, adapter_id, K, D, r, 2.0 * r, False)
 
 
@@ -354,11 +393,12 @@ class LazyAdapter:
         return mixed_adapter(self.seed, self.layer, self.module, self.adapter_id, K, D)
 
 
-def mixed(n_layers: int = 32) -> Workload:
+def mixed(n_layers: int = 32, classes: bool = True) -> Workload:
     """The mixed serving step as a workload whose tensors are generated on demand: linears
     layer-major over MIXED_MODULES (x_id = linear index), adapters as LazyAdapter, W = None and
-    no xs entries (see materialize_linear / materialize_x)."""
-    plan = mixed_step_plan()
+    no xs entries (see materialize_linear / materialize_x). With classes (default) the pools'
+    128 slots come in rank classes 8 / 16 / 64 (mixed_step_plan)."""
+    plan = mixed_step_plan(classes=classes)
     seed = plan["seed"]
     linears = []
     for l in range(n_layers):
@@ -368,8 +408,10 @@ def mixed(n_layers: int = 32) -> Workload:
                 r = plan["rank_of"][a]
                 lin.adapters[s] = LazyAdapter(seed, l, m, a, r, 2.0 * r, False)
             linears.append(lin)
+    n_pre = plan["n_prefill_tokens"]
     return Workload("mixed", seed, plan["T"], 1, 128, 64, plan["token_slots"], None, {}, linears,
-                    notes="tensors generated on demand by layer and module")
+                    notes="tensors generated on demand by layer and module",
+                    phases=[("prefill", 0, n_pre), ("decode", n_pre, plan["T"])], classes=plan["classes"])
 
 
 def _layer_module(wl: Workload, lin: Linear) -> tuple:

@@ -54,7 +54,7 @@ class DeviceWorkload:
         self.linears = []
         for lin in (wl.linears if linears is None else linears):
             lazy = lin.W is None                  # the mixed step: tensors generated here, per linear
-            pool = layer.AdapterPool(wl.n_slots, wl.r_max, lin.K, lin.D)
+            pool = layer.AdapterPool(wl.n_slots, wl.r_max, lin.K, lin.D, classes=getattr(wl, "classes", None))
             for s, ad in lin.adapters.items():
                 if isinstance(ad, synth.LazyAdapter):
                     ad = ad.materialize(lin.K, lin.D)
@@ -78,15 +78,58 @@ class DeviceWorkload:
         for dl in self.linears:
             self.layer.linear(dl.pool, self.meta, self.x[dl.lin.x_id], dl.W, dl.y, stream)
 
+    def sub_rows(self, r0: int, r1: int) -> "RowRange":
+        """The same linears (pools, W) over token rows [r0, r1): a phase of the step."""
+        return RowRange(self, r0, r1)
+
     def close(self):
         for dl in self.linears:
             dl.pool.close()
         self.meta.close()
 
 
+class RowRange:
+    """Token rows [r0, r1) of a DeviceWorkload through all of its linears, with metadata of their
+    own (x and y are row slices of the workload's tensors)."""
+
+    def __init__(self, dw: DeviceWorkload, r0: int, r1: int):
+        self.dw, self.r0, self.r1 = dw, r0, r1
+        self.meta = dw.layer.StepMeta(r1 - r0, dw.wl.J, dw.wl.r_max)
+        self.token_slots = dw.token_slots[r0:r1].contiguous()
+        self.scales = None if dw.scales is None else dw.scales[r0:r1].contiguous()
+
+    def run(self, stream=None):
+        dw = self.dw
+        self.meta.build(self.token_slots, self.scales, dw.linears[0].pool, stream)
+        for dl in dw.linears:
+            dw.layer.linear(dl.pool, self.meta, dw.x[dl.lin.x_id][self.r0:self.r1], dl.W, dl.y[self.r0:self.r1],
+                            stream)
+
+    def close(self):
+        self.meta.close()
+
+
 def oracle_rows(wl: synth.Workload, lin: synth.Linear, rows=None, cols=None, threads=None) -> np.ndarray:
     return oracle.linear(wl.xs[lin.x_id], lin.W, wl.token_slots, lin.adapters, wl.n_slots, scales=wl.scales,
                          rows=rows, cols=cols, threads=threads)
+
+
+def tile_rows(wl: synth.Workload, per_tile: int = 1, seed: int = 0) -> np.ndarray:
+    """Token rows covering every 128-token tile (per_tile random rows each, plus the tile's
+    first and last row) and the first token of every slot in use (sorted)."""
+    rng = np.random.default_rng(seed)
+    picks = set()
+    for t0 in range(0, wl.T, 128):
+        t1 = min(wl.T, t0 + 128)
+        picks.update((t0, t1 - 1))
+        picks.update(int(t) for t in rng.integers(t0, t1, size=per_tile))
+    first = {}
+    for t in range(wl.T):
+        for s in wl.token_slots[t]:
+            if s >= 0:
+                first.setdefault(int(s), t)
+    picks.update(first.values())
+    return np.array(sorted(picks), dtype=np.int64)
 
 
 def sample_rows(wl: synth.Workload, n: int, seed: int = 0) -> np.ndarray:

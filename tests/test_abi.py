@@ -61,7 +61,9 @@ def test_pool_bytes_reproduces_the_pages_slot_figures(lib):
         elif key == "hundred_rank16_gib":
             assert round(model_slots(100, 16) / GiB, int(v[1])) == float(v[0])
     assert mlora.mlora_pool_bytes(0, 8, 64, 64) == 0
-    assert mlora.mlora_pool_bytes(1, 5, 64, 64) == 1 * 8 * 128 * 2      # rank width padded to 8
+    assert mlora.mlora_pool_bytes(1, 5, 64, 64) == 1 * 8 * 128 * 2      # slot width 8
+    assert mlora.mlora_pool_bytes(2, 24, 64, 64) == 2 * 32 * 128 * 2     # 8, 16, 32, 64 ...
+    assert mlora.mlora_pool_bytes(1, 100, 64, 64) == 1 * 128 * 128 * 2   # ... then multiples of 64
 
 
 def test_status_strings(lib):

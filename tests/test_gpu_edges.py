@@ -61,8 +61,8 @@ def test_eight_slots_per_token_and_the_largest_rank(cuda_device):
 
 @pytest.mark.parametrize("T", [256, 257])
 def test_small_batch_switch(cuda_device, T):
-    # 256 tokens take the fused small-batch path, 257 the large-batch path (rank width 64: the
-    # tensor-core prefill path with every tile overflowing to the CUDA-core kernels)
+    # 256 tokens take the fused small-batch path, 257 the tensor-core side path (three M-tiles of
+    # per-token random slots)
     wl = _workload(f"switch-{T}", 30 + T, T=T, K=520, D=264, S=20, R=64, J=1,
                    ranks=lambda s, rng: (8, 16, 64)[s % 3])
     _run_and_check(wl)

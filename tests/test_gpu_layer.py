@@ -9,7 +9,7 @@ import pytest
 import oracle
 import synth
 from tests.conftest import read_golden
-from tests.harness import DeviceWorkload, assert_close, errors, oracle_rows, sample_rows
+from tests.harness import DeviceWorkload, assert_close, errors, oracle_rows, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -110,14 +110,34 @@ def test_ragged_multi_slot_cases(cuda_device, T, K, D, S, R, J, seed):
 
 
 def test_decode_config_full_size(cuda_device):
+    # every token row of every linear
     wl = synth.decode()
     dw = DeviceWorkload(wl)
     dw.run()
     dw.meta.status()
-    rows = sample_rows(wl, 24)
     for dl in dw.linears:
-        _check_linear(wl, dw, dl, rows=rows)
+        _check_linear(wl, dw, dl)
     dw.close()
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_decode_shapes_on_both_paths(cuda_device, path):
+    """The decode configuration's shapes forced onto the small-batch path (1) and onto the
+    tensor-core side path (2): both against the oracle on sampled rows."""
+    from rank_adapter_gemm_token_gb300 import mlora
+    wl = synth.decode()
+    wl.linears = wl.linears[:2]
+    mlora.mlora_set_path(path)
+    try:
+        dw = DeviceWorkload(wl)
+        dw.run()
+        dw.meta.status()
+        rows = sample_rows(wl, 40)
+        for dl in dw.linears:
+            _check_linear(wl, dw, dl, rows=rows)
+        dw.close()
+    finally:
+        mlora.mlora_set_path(0)
 
 
 def test_compose_config_full_size(cuda_device):
@@ -125,8 +145,7 @@ def test_compose_config_full_size(cuda_device):
     dw = DeviceWorkload(wl)
     dw.run()
     dw.meta.status()
-    rows = sample_rows(wl, 32)
-    _check_linear(wl, dw, dw.linears[0], rows=rows)
+    _check_linear(wl, dw, dw.linears[0])                     # every token row
     # RFC 51940, Testing: the fused k-slot pass equals running one slot at a time and accumulating.
     import torch
     from rank_adapter_gemm_token_gb300 import layer
@@ -144,11 +163,13 @@ def test_compose_config_full_size(cuda_device):
 
 
 def test_prefill_config_full_size(cuda_device):
+    # rows in every one of the 32 tiles (first, last and two more) and of every slot
     wl = synth.prefill()
     dw = DeviceWorkload(wl)
     dw.run()
     dw.meta.status()
-    rows = sample_rows(wl, 16)
+    rows = tile_rows(wl, per_tile=2)
+    assert len(set(int(r) // 128 for r in rows)) == (wl.T + 127) // 128
     for dl in dw.linears:
         _check_linear(wl, dw, dl, rows=rows)
     dw.close()
@@ -245,12 +266,12 @@ def test_clear_slot_makes_it_empty(cuda_device):
                                               (1, 7, 1900, 328, 2504, 0), (2, 8, 1900, 328, 2504, 0),
                                               (1, 9, 1900, 328, 2504, 224), (2, 10, 1500, 200, 1000, 128),
                                               (1, 11, 1500, 200, 1000, 256)])
-def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed, T, K, D, bn):
-    """T > 256 with r_max 64: runs of one slot (M-tiles with at most 4 slots: shrink on the tensor
-    cores, expand inside the base GEMM) followed by per-token random slots (tiles with more
-    slots: CUDA-core path). Ragged T, K and D; mixed ranks; a second slot per token for J = 2.
+def test_tensor_core_path_runs_then_random_slots(cuda_device, J, seed, T, K, D, bn):
+    """T > 256 with r_max 64: runs of one slot (M-tiles with one or two units) followed by per-token
+    random slots (tiles with many units); all on the tensor-core side path (shrink per unit, expand
+    inside the base GEMM). Ragged T, K and D; mixed ranks; a second slot per token for J = 2.
     The 1900 x 2504 cases have enough 256 x 256 tiles for the CTA-pair GEMM, an odd number of
-    128-row M-tiles (the last pair tile has one) and pairs of M-tiles with different slot lists."""
+    128-row M-tiles (the last pair tile has one) and pairs of M-tiles with different unit lists."""
     rng = np.random.default_rng(seed)
     S, R = 12, 64
     seg_end = 5 * T // 7
@@ -286,11 +307,10 @@ def test_tensor_core_prefill_path_with_overflow_tiles(cuda_device, J, seed, T, K
 
 @pytest.mark.parametrize("J,seed,T,ovf", [(1, 50, 700, (4, 5)), (2, 51, 700, (4, 5)), (1, 52, 900, (1, 5)),
                                           (1, 53, 640, (2,)), (2, 54, 1100, (0, 8))])
-def test_overflow_window(cuda_device, J, seed, T, ovf):
+def test_tiles_with_many_slots(cuda_device, J, seed, T, ovf):
     """T > 256, rank width 64: the tiles listed in ovf draw a slot per token from 40 adapters
-    (more than 4 slots per tile: the overflow window, handled by the small-batch shrink and
-    expand over those 256 tokens), the others use runs of one slot (tensor-core path). Covers
-    one and two window tiles, adjacent or not, a ragged last tile, and J = 2."""
+    (tens of units per tile), the others use runs of one slot. Covers one and two such tiles,
+    adjacent or not, a ragged last tile, and J = 2."""
     rng = np.random.default_rng(seed)
     K, D, S, R = 320, 392, 40, 64
     lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
@@ -310,7 +330,7 @@ def test_overflow_window(cuda_device, J, seed, T, ovf):
             slots[t0:t0 + 70, 0] = int(rng.integers(0, S))
             slots[t0 + 70:t1, 0] = int(rng.integers(-1, S))
     scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
-    wl = synth.Workload("overflow-window", seed, T, J, S, R, slots, scales,
+    wl = synth.Workload("many-slots", seed, T, J, S, R, slots, scales,
                         {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
     dw = DeviceWorkload(wl)
     dw.run()
@@ -401,4 +421,102 @@ def test_separate_gemm_shrink_expand_entry_points(cuda_device, T, J, R, seed):
     torch.cuda.synchronize()
     dw.meta.status()
     assert_close(y.cpu().numpy(), oracle_rows(wl, lin), "separate entry points")
+    dw.close()
+
+
+def _classed_workload(name, seed, T, J, classes, K, D, runs=False):
+    """Adapters of a classed pool: slots numbered class by class, each adapter's rank at most its
+    class's rank (some at it); tokens draw random slots (or runs of one slot)."""
+    rng = np.random.default_rng(seed)
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    s = 0
+    for n, rc in classes:
+        for i in range(n):
+            r = rc if i % 2 == 0 else int(rng.integers(1, rc + 1))
+            lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                            B=synth.normal_bf16(seed, 3000 + s, (D, r), 0.02),
+                                            rank=r, alpha=float(2 * r), rslora=bool(s % 3 == 0))
+            s += 1
+    S = s
+    if runs:
+        slots = np.repeat(rng.integers(-1, S, size=(T + 95) // 96), 96)[:T].reshape(T, 1).astype(np.int32)
+        slots = np.concatenate([slots] + [rng.integers(-1, S, size=(T, 1)).astype(np.int32)] * (J - 1), axis=1)
+    else:
+        slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload(name, seed, T, J, S, max(r for _, r in classes), slots, scales,
+                        {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
+    wl.classes = list(classes)
+    return wl
+
+
+@pytest.mark.parametrize("T,J,classes,K,D,runs,seed", [
+    (64, 1, [(5, 8), (4, 16), (3, 64)], 256, 200, False, 80),          # one M-tile: one-CTA GEMM
+    (200, 2, [(7, 8), (6, 16), (5, 64)], 320, 392, False, 81),         # two M-tiles: CTA pairs
+    (700, 1, [(43, 8), (43, 16), (42, 64)], 256, 520, True, 82),       # the mixed step's classes
+    (900, 3, [(9, 8), (3, 24), (4, 100), (2, 256)], 136, 264, False, 83),   # widths 8 / 32 / 128 / 256
+])
+def test_rank_class_pools(cuda_device, T, J, classes, K, D, runs, seed):
+    """Pools whose slots come in rank classes (compact columns: a rank-8 slot is 8 columns wide,
+    eight of them share a 64-column block) against the oracle, on the tensor-core side path."""
+    wl = _classed_workload("classes", seed, T, J, classes, K, D, runs)
+    dw = DeviceWorkload(wl)
+    lay = dw.linears[0].pool.layout()
+    widths = [w for n, r in classes for w in [{8: 8, 16: 16, 24: 32, 64: 64, 100: 128, 256: 256}[r]] * n]
+    assert lay["slot_width"] == widths
+    assert all(off % min(w, 64) == 0 for off, w in zip(lay["slot_off"], lay["slot_width"]))
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
+    dw.close()
+
+
+def test_rank_class_limits_and_mismatch(cuda_device):
+    import torch
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+    pool = layer.AdapterPool(0, 0, 64, 32, classes=[(2, 8), (2, 16)])
+    A, B = np.zeros((16, 64), np.uint16), np.zeros((32, 16), np.uint16)
+    with pytest.raises(mlora.MloraError) as e:               # slot 1 is a rank-8 slot
+        mlora.mlora_load_adapter(pool.handle, 1, A, B, 16, 32.0, False)
+    assert e.value.status == mlora.MLORA_ERR_RANK_TOO_LARGE and "16" in str(e.value) and "8" in str(e.value)
+    mlora.mlora_load_adapter(pool.handle, 2, A, B, 16, 32.0, False)     # a rank-16 slot
+    other = layer.AdapterPool(4, 16, 64, 32)                 # same slot count, one class
+    meta = layer.StepMeta(8, 1, 16)
+    meta.build(torch.full((8, 1), -1, dtype=torch.int32, device="cuda"), None, pool)
+    x = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((32, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mlora.MloraError) as e:
+        layer.linear(other, meta, x, W)
+    assert e.value.status == mlora.MLORA_ERR_MISMATCH
+    for bad in ([(0, 8)], [(2, 0)], [(2, 300)], [(1, 8)] * 9):
+        with pytest.raises(mlora.MloraError) as e:
+            layer.AdapterPool(0, 0, 64, 32, classes=bad)
+        assert e.value.status == mlora.MLORA_ERR_INVALID_ARG
+    meta.close()
+    other.close()
+    pool.close()
+
+
+def test_tiles_past_the_unit_limit_take_the_cuda_core_kernels(cuda_device):
+    """J = 8 over 300 rank-64 slots: an M-tile's pairs use more than 256 of the 300 column blocks,
+    so the tile overflows the unit lists and its pairs take the CUDA-core shrink and expand; a
+    run of one slot keeps other tiles on the tensor cores."""
+    rng = np.random.default_rng(90)
+    T, J, S, R, K, D = 400, 8, 300, 64, 128, 136
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(90, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = int(rng.integers(1, R + 1))
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(90, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(90, 3000 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(2 * r), rslora=bool(s % 2))
+    slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    slots[:128] = -1
+    slots[:128, 0] = 7                                           # tile 0: one unit
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("unit-overflow", 90, T, J, S, R, slots, scales,
+                        {0: synth.normal_bf16(90, 11, (T, K), 1.0)}, [lin])
+    dw = DeviceWorkload(wl)
+    dw.run()
+    dw.meta.status()
+    _check_linear(wl, dw, dw.linears[0])
     dw.close()
