@@ -122,9 +122,10 @@ MLORA_API mlora_status mlora_pool_destroy(mlora_pool_t pool);
  *   message naming both ranks), alpha finite.
  *   rslora != 0 selects c = alpha / sqrt(rank), else c = alpha / rank.
  * Runs on the pool's copy stream after every mlora_linear already issued on this pool
- * (write-after-read ordering by event): the slot's columns are zeroed, A is copied to rows
- * off_s .. off_s + rank - 1 of A_pool, B to columns off_s .. of B_pool (a strided copy, row
- * pitch C). Returns when the copies are queued; with pinned
+ * (write-after-read ordering by event): the slot's A rows are zeroed and A is copied to rows
+ * off_s .. off_s + rank - 1 of A_pool; B is copied whole into a staging buffer of the pool and a
+ * kernel writes it to columns off_s .. off_s + R_s - 1 of B_pool (zeros past the rank). Returns
+ * when the copies are queued; with pinned
  * host buffers they are asynchronous and the buffers must stay valid until
  * mlora_pool_sync() or the next mlora_linear on this pool has been ordered after them.
  * With pageable buffers the copy is complete on return. */

@@ -18,7 +18,7 @@ constexpr int kMaxTiles = 512;         // 128-token M-tiles of a step (65535 tok
 constexpr int kBlockCols = 64;         // columns of the slot space per extra K block (one 128-byte row)
 constexpr int kMaxTileUnits = 256;     // (M-tile, column block) units of one M-tile on the tensor cores
 constexpr int kMaxUnits = 16384;       // units of one step on the tensor cores (v tiles of 16 KB each)
-constexpr int kGroupUnits = 4;         // units of one M-tile shrunk together (MMA N = 64 per unit)
+constexpr int kGroupUnits = 4;         // pair-tile entries shrunk together (MMA N = 64 per entry)
 
 // Columns a slot of maximum rank r owns: 8, 16, 32 or 64, or a multiple of 64 above that, so that
 // with each class starting on a multiple of min(width, 64) no slot straddles two 64-column blocks.
@@ -67,9 +67,11 @@ struct MetaView {
   int32_t* tile_unit_off; // [tiles + 1] units of tile i: [tile_unit_off[i], tile_unit_off[i + 1])
   int32_t* unit_blk;      // [U] column block of each unit
   int32_t* unit_tile;     // [U] M-tile of each unit
-  int32_t* grp_unit;      // [U] shrink groups: first unit (kGroupUnits consecutive units of one tile)
-  int32_t* grp_cnt;       // [U] units in the group
-  int32_t* ptile_off;     // [pair tiles + 1] entries of pair tile mp (M-tiles 2mp, 2mp + 1)
+  int32_t* grp_mp;        // [U] shrink groups: pair tile of the group
+  int32_t* grp_ent;       // [U]   first pair-tile entry (kGroupUnits consecutive entries of one pair tile)
+  int32_t* grp_cnt;       // [U]   entries in the group
+  int32_t* ptile_off;     // [pair tiles + 1] entries of pair tile mp (M-tiles 2mp, 2mp + 1), the union
+                          //   of both tiles' units by block
   int32_t* pent_blk;      // [U] column block of each pair-tile entry (ascending within a pair tile)
   int32_t* pent_u0;       // [U] unit of M-tile 2mp with that block (-1: none)
   int32_t* pent_u1;       // [U] unit of M-tile 2mp + 1 with that block (-1: none)

@@ -71,20 +71,27 @@ __device__ __forceinline__ int warp_exclusive(int c, int* total) {
 }
 
 // Bitmap (n_words words) of the column blocks owned by the slots of M-tile `tile`'s active pairs;
-// one warp. A slot of width w at column offset off covers blocks off / 64 .. (off + w - 1) / 64.
+// one warp. slot_blk[s] holds the first block of slot s in its low 16 bits and the last in its
+// high 16 bits (a slot of width w at column offset off covers blocks off / 64 .. (off + w - 1) / 64).
 __device__ __forceinline__ void tile_block_bitmap(uint32_t* bm, int n_words, int tile, int T, int J,
-                                                  const int* pslot, const int32_t* slot_off,
-                                                  const int32_t* slot_width) {
+                                                  const int* pslot, const uint32_t* slot_blk) {
   const int lane = threadIdx.x & 31;
   for (int k = lane; k < n_words; k += 32) bm[k] = 0u;
   __syncwarp();
+  // pairs of one slot share their blocks: per round of 32 pairs one lane per distinct slot sets
+  // the bits, and only bits not yet set cost an atomic (the words are few and heavily shared)
   const int p0 = tile * 128 * J, p1 = min(T, tile * 128 + 128) * J;
-  for (int p = p0 + lane; p < p1; p += 32) {
-    const int s = pslot[p];
-    if (s < 0) continue;
-    const int off = slot_off[s];
-    const int b1 = (off + slot_width[s] - 1) / kBlockCols;
-    for (int b = off / kBlockCols; b <= b1; ++b) atomicOr(&bm[b >> 5], 1u << (b & 31));
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const int s = p < p1 ? pslot[p] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, s);
+    if (s >= 0 && lane == __ffs(peers) - 1) {
+      const uint32_t sb = slot_blk[s];
+      for (int b = static_cast<int>(sb & 0xFFFFu); b <= static_cast<int>(sb >> 16); ++b) {
+        const uint32_t bit = 1u << (b & 31);
+        if (!(bm[b >> 5] & bit)) atomicOr(&bm[b >> 5], bit);
+      }
+    }
   }
   __syncwarp();
 }
@@ -106,9 +113,11 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem);
   const size_t bins_bytes = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
   const size_t bm_bytes = static_cast<size_t>(32) * 2 * n_words * sizeof(uint32_t);
+  const size_t front = ((bins_bytes > bm_bytes ? bins_bytes : bm_bytes) + 15) / 16 * 16;
+  uint32_t* slot_blk = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(smem) + front);   // [S]
   // small steps keep their pair slots, order and pair-blocks in shared memory as well, so the
   // later steps read them there instead of going back to global memory
-  int* c_base = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(smem) + ((bins_bytes > bm_bytes ? bins_bytes : bm_bytes) + 15) / 16 * 16);
+  int* c_base = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(smem) + front + (static_cast<size_t>(S) * 4 + 15) / 16 * 16);
   int* pslot = cache ? c_base : m.pair_slot;            // [n] validated slot per pair
   int* ord = cache ? c_base + n : m.order;              // [n] sorted pair order
   int* bstart = cache ? c_base + 2 * n : m.blk_start;   // [n] pair-block starts
@@ -118,7 +127,6 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __shared__ int n_blk_sh;                               // pair-blocks in total
   __shared__ int tile_cnt[kMaxTiles];                    // units per 128-token M-tile (0 if it overflows)
   __shared__ int tile_off[kMaxTiles + 1];                // first unit of each M-tile
-  __shared__ int tile_grp[kMaxTiles];                    // first shrink group of each M-tile
   __shared__ uint8_t tile_ovf[kMaxTiles];                // 1: the tile's pairs take the CUDA-core kernels
   __shared__ int ptile_cnt[kMaxTiles / 2];               // entries per pair tile
 
@@ -131,7 +139,12 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   //    `cursor` is free until step 2
   for (int b = tid; b < nb; b += kMetaThreads) {
     hist[b] = 0;
-    if (b < S) cursor[b] = pool.slot_rank[b] > 0;
+    if (b < S) {
+      cursor[b] = pool.slot_rank[b] > 0;
+      const int off = pool.slot_off[b];
+      slot_blk[b] = static_cast<uint32_t>(off / kBlockCols) |
+                    (static_cast<uint32_t>((off + pool.slot_width[b] - 1) / kBlockCols) << 16);
+    }
   }
   if (tid == 0) first_bad = INT_MAX;
   __syncthreads();
@@ -242,7 +255,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   uint32_t* bmA = bitmaps + warp * 2 * n_words;
   uint32_t* bmB = bmA + n_words;
   for (int i = warp; i < n_tiles; i += 32) {
-    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, slot_blk);
     int c = 0;
     for (int w = lane; w < n_words; w += 32) c += __popc(bmA[w]);
 #pragma unroll
@@ -260,12 +273,11 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     block_exclusive_scan3(capped, 0, 0, off, unused0, unused1, warp_sums);
     const bool ovf = c > kMaxTileUnits || off + capped > m.unit_cap;
     const int fin = ovf ? 0 : c;
-    int uoff, goff;
-    block_exclusive_scan3(fin, (fin + kGroupUnits - 1) / kGroupUnits, 0, uoff, goff, unused1, warp_sums);
+    int uoff;
+    block_exclusive_scan3(fin, 0, 0, uoff, unused0, unused1, warp_sums);
     if (tid < n_tiles) {
       tile_cnt[tid] = fin;
       tile_off[tid] = uoff;
-      tile_grp[tid] = goff;
       tile_ovf[tid] = ovf ? 1 : 0;
       m.tile_unit_off[tid] = uoff;
     }
@@ -273,7 +285,6 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
       tile_off[n_tiles] = uoff + fin;
       m.tile_unit_off[n_tiles] = uoff + fin;
       m.counts[6] = uoff + fin;
-      m.counts[7] = goff + (fin + kGroupUnits - 1) / kGroupUnits;
     }
     if (n_tiles == 0 && tid == 0) {
       m.tile_unit_off[0] = 0;
@@ -282,11 +293,11 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     }
   }
   __syncthreads();
-  // units in ascending block order per tile, and the shrink's groups of consecutive units
+  // units in ascending block order per tile
   for (int i = warp; i < n_tiles; i += 32) {
     const int cnt = tile_cnt[i];
     if (cnt == 0) continue;
-    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, slot_blk);
     const int ubase = tile_off[i];
     int run = 0;
     for (int k0 = 0; k0 < n_words; k0 += 32) {
@@ -303,18 +314,14 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
       }
       run += total;
     }
-    for (int g = lane; g * kGroupUnits < cnt; g += 32) {
-      m.grp_unit[tile_grp[i] + g] = ubase + g * kGroupUnits;
-      m.grp_cnt[tile_grp[i] + g] = min(kGroupUnits, cnt - g * kGroupUnits);
-    }
   }
   // pair tiles (M-tiles 2 mp and 2 mp + 1): the union of both tiles' blocks, each entry with the
   // unit of either tile on that block (-1 where the tile does not use it)
   for (int mp = warp; mp < n_ptiles; mp += 32) {
     const int ta = 2 * mp, tb = 2 * mp + 1;
     const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
-    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
-    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, slot_blk);
+    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, slot_blk);
     int c = 0;
     for (int w = lane; w < n_words; w += 32) c += __popc((ha ? bmA[w] : 0u) | (hb ? bmB[w] : 0u));
 #pragma unroll
@@ -324,12 +331,22 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   }
   __syncthreads();
   {
+    // entries of each pair tile, and the shrink's groups of kGroupUnits consecutive entries
     const int c = tid < n_ptiles ? ptile_cnt[tid] : 0;
-    int off, unused0, unused1;
-    block_exclusive_scan3(c, 0, 0, off, unused0, unused1, warp_sums);
+    const int ng = (c + kGroupUnits - 1) / kGroupUnits;
+    int off, goff, unused1;
+    block_exclusive_scan3(c, ng, 0, off, goff, unused1, warp_sums);
     if (tid < n_ptiles) m.ptile_off[tid] = off;
-    if (tid == n_ptiles - 1) m.ptile_off[n_ptiles] = off + c;
+    if (tid == n_ptiles - 1) {
+      m.ptile_off[n_ptiles] = off + c;
+      m.counts[7] = goff + ng;
+    }
     if (n_ptiles == 0 && tid == 0) m.ptile_off[0] = 0;
+    for (int g = 0; g < ng; ++g) {
+      m.grp_mp[goff + g] = tid;
+      m.grp_ent[goff + g] = off + g * kGroupUnits;
+      m.grp_cnt[goff + g] = min(kGroupUnits, c - g * kGroupUnits);
+    }
     if (tid < n_ptiles) ptile_cnt[tid] = off;          // from here: first entry of the pair tile
   }
   __syncthreads();
@@ -337,8 +354,8 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     const int ta = 2 * mp, tb = 2 * mp + 1;
     const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
     if (!ha && !hb) continue;
-    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
-    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, pool.slot_off, pool.slot_width);
+    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, slot_blk);
+    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, slot_blk);
     int ra = 0, rb = 0, ru = 0;
     const int ua = tile_off[ta], ub = hb ? tile_off[tb] : 0, ebase = ptile_cnt[mp];
     for (int k0 = 0; k0 < n_words; k0 += 32) {
@@ -402,7 +419,7 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
   const size_t bins = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
   const size_t n_words = (static_cast<size_t>(pool.C) + kBlockCols * 32 - 1) / (kBlockCols * 32);
   const size_t bitmaps = 32 * 2 * n_words * sizeof(uint32_t);
-  const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16;
+  const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16 + (static_cast<size_t>(pool.S) * 4 + 15) / 16 * 16;
   if (front > kMetaMaxDynSmem) return cudaErrorInvalidValue;
   const int cache = front + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
   const size_t smem = front + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);

@@ -106,6 +106,41 @@ __global__ void set_slot_kernel(float* slot_scale, int32_t* slot_rank, int slot,
   slot_rank[slot] = rank;
 }
 
+// Row ranges of the slices of a slot being loaded (a plain adapter is one slice of all D rows).
+struct SliceRows {
+  int n;
+  int row0[MLORA_MAX_SLICES + 1];       // slice i covers rows row0[i] .. row0[i + 1] - 1
+};
+
+// Writes a slot's columns of B from the staged adapter: element (o, q), q < width, is slice i's
+// B[o - row0[i]][q - i r] when o lies in slice i and q in its columns i r .. i r + r - 1, else 0.
+// stage holds the slices one after another, each [rows_i, r] row-major. Thread = (row, 8 columns).
+__global__ void scatter_slot_b_kernel(uint16_t* __restrict__ B, int C, int off, int width, int D,
+                                      const uint16_t* __restrict__ stage, int r, SliceRows sl) {
+  const int groups = width / 8;
+  const long items = static_cast<long>(D) * groups;
+  for (long it = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; it < items;
+       it += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int o = static_cast<int>(it / groups), q0 = static_cast<int>(it % groups) * 8;
+    int i = 0;
+    while (i + 1 < sl.n && o >= sl.row0[i + 1]) ++i;
+    uint16_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int q = q0 + k - i * r;
+      v[k] = (i < sl.n && q >= 0 && q < r)
+                 ? stage[static_cast<size_t>(sl.row0[i]) * r + static_cast<size_t>(o - sl.row0[i]) * r + q]
+                 : static_cast<uint16_t>(0);
+    }
+    uint4 w;
+    w.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+    w.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+    w.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+    w.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+    *reinterpret_cast<uint4*>(B + static_cast<size_t>(o) * C + off + q0) = w;
+  }
+}
+
 }  // namespace
 
 namespace mlora {
@@ -146,6 +181,7 @@ struct mlora_pool {
   int32_t* slot_off = nullptr;                 // [S] first column of each slot
   int32_t* slot_width = nullptr;               // [S] columns of each slot
   int32_t* col_slot = nullptr;                 // [C] slot owning each column
+  uint16_t* stage = nullptr;                   // [D * R] a loading adapter's B, before its scatter
   std::vector<int> class_slots, class_rank;    // the rank classes (one for mlora_pool_create)
   std::vector<int> h_rank, h_off, h_width, h_class;
   int max_span = 1;                            // most 64-column blocks one slot touches
@@ -178,8 +214,8 @@ struct mlora_meta {
   float* vpart = nullptr;
   float* vfull = nullptr;
   int vfull_ld = 0;
-  int32_t *tile_unit_off = nullptr, *unit_blk = nullptr, *unit_tile = nullptr, *grp_unit = nullptr,
-          *grp_cnt = nullptr, *ptile_off = nullptr, *pent_blk = nullptr, *pent_u0 = nullptr, *pent_u1 = nullptr,
+  int32_t *tile_unit_off = nullptr, *unit_blk = nullptr, *unit_tile = nullptr, *grp_mp = nullptr,
+          *grp_ent = nullptr, *grp_cnt = nullptr, *ptile_off = nullptr, *pent_blk = nullptr, *pent_u0 = nullptr, *pent_u1 = nullptr,
           *pair_fused = nullptr, *todo_blk = nullptr;
   uint16_t* vtile = nullptr;
   int unit_cap = 0;
@@ -209,7 +245,8 @@ struct mlora_meta {
     v.tile_unit_off = tile_unit_off;
     v.unit_blk = unit_blk;
     v.unit_tile = unit_tile;
-    v.grp_unit = grp_unit;
+    v.grp_mp = grp_mp;
+    v.grp_ent = grp_ent;
     v.grp_cnt = grp_cnt;
     v.ptile_off = ptile_off;
     v.pent_blk = pent_blk;
@@ -351,7 +388,8 @@ static mlora_status pool_create(int n_classes, const int* class_slots, const int
       (e = cudaMalloc(&p->slot_rank, p->S * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->slot_off, p->S * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->slot_width, p->S * sizeof(int32_t))) != cudaSuccess ||
-      (e = cudaMalloc(&p->col_slot, p->C * sizeof(int32_t))) != cudaSuccess) {
+      (e = cudaMalloc(&p->col_slot, p->C * sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMalloc(&p->stage, static_cast<size_t>(D) * p->R * 2)) != cudaSuccess) {
     cudaGetLastError();
     mlora_pool_destroy(p);
     return e == cudaErrorMemoryAllocation ? fail(MLORA_ERR_OOM, "cudaMalloc of %zu + %zu bytes failed", a_bytes, b_bytes)
@@ -428,15 +466,17 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
   cudaFree(p->slot_off);
   cudaFree(p->slot_width);
   cudaFree(p->col_slot);
+  cudaFree(p->stage);
   delete p;
   return MLORA_OK;
 }
 
 // Writes a slot on the pool's copy stream after every call already queued on the pool: zeroes
-// its columns (rows off .. off + width - 1 of A, columns off .. of B), then copies n_slices
-// adapters of rank r each; slice i's A [r, K] goes to rows off + i r .. and its B [widths[i], r]
-// to rows o_i .. (o_i = sum of the earlier widths) and columns off + i r .. of B (block-diagonal; a
-// plain adapter is one slice of width D). n_slices = 0 clears it.
+// its A rows (rows off .. off + width - 1) and copies n_slices adapters of rank r each; slice i's
+// A [r, K] goes to rows off + i r ..; the slices' B [widths[i], r] are copied whole into the
+// pool's staging buffer and a kernel writes the slot's B columns off .. off + width - 1 from it
+// (slice i at rows o_i .. (o_i = sum of the earlier widths) and columns off + i r .., zeros
+// elsewhere: block-diagonal; a plain adapter is one slice of width D). n_slices = 0 clears it.
 static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, const int* widths,
                                       const mlora_bf16* const* A_host, const mlora_bf16* const* B_host, int r,
                                       float alpha, int rslora) {
@@ -447,22 +487,32 @@ static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, co
   }
   const size_t off = static_cast<size_t>(p->h_off[slot]);
   const size_t width = static_cast<size_t>(p->h_width[slot]);
-  const size_t pitch = static_cast<size_t>(p->C) * 2;
   uint16_t* a_slot = p->A + off * p->K;
-  uint16_t* b_slot = p->B + off;
   MLORA_CUDA(cudaMemsetAsync(a_slot, 0, width * p->K * 2, cs), "zero slot A");
-  MLORA_CUDA(cudaMemset2DAsync(b_slot, pitch, 0, width * 2, static_cast<size_t>(p->D), cs), "zero slot B");
+  SliceRows sl{};
+  sl.n = n_slices;
   int row = 0;
   for (int i = 0; i < n_slices; ++i) {
     const int w = widths ? widths[i] : p->D;
+    sl.row0[i] = row;
     MLORA_CUDA(cudaMemcpyAsync(a_slot + static_cast<size_t>(i) * r * p->K, A_host[i], static_cast<size_t>(r) * p->K * 2,
                                cudaMemcpyHostToDevice, cs),
                "copy A into slot");
-    MLORA_CUDA(cudaMemcpy2DAsync(b_slot + static_cast<size_t>(row) * p->C + static_cast<size_t>(i) * r, pitch, B_host[i],
-                                 static_cast<size_t>(r) * 2, static_cast<size_t>(r) * 2, static_cast<size_t>(w),
-                                 cudaMemcpyHostToDevice, cs),
-               "copy B into slot");
+    MLORA_CUDA(cudaMemcpyAsync(p->stage + static_cast<size_t>(row) * r, B_host[i], static_cast<size_t>(w) * r * 2,
+                               cudaMemcpyHostToDevice, cs),
+               "copy B to the staging buffer");
     row += w;
+  }
+  sl.row0[n_slices] = row;
+  {
+    const long items = static_cast<long>(p->D) * static_cast<long>(width / 8);
+    const int grid = static_cast<int>(std::min<long>((items + 255) / 256, 4096));
+    note_launch_begin(kKindSlot, cs);
+    scatter_slot_b_kernel<<<grid, 256, 0, cs>>>(p->B, p->C, static_cast<int>(off), static_cast<int>(width), p->D,
+                                                p->stage, r, sl);
+    cudaError_t e = cudaGetLastError();
+    note_launch_end(kKindSlot, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter_slot_b_kernel");
   }
   const int rank = n_slices * r;
   note_launch_begin(kKindSlot, cs);
@@ -619,7 +669,8 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->tile_unit_off), (n_tiles + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->unit_blk), U * 4);
   alloc(reinterpret_cast<void**>(&m->unit_tile), U * 4);
-  alloc(reinterpret_cast<void**>(&m->grp_unit), U * 4);
+  alloc(reinterpret_cast<void**>(&m->grp_mp), U * 4);
+  alloc(reinterpret_cast<void**>(&m->grp_ent), U * 4);
   alloc(reinterpret_cast<void**>(&m->grp_cnt), U * 4);
   alloc(reinterpret_cast<void**>(&m->ptile_off), ((n_tiles + 1) / 2 + 1) * 4);
   alloc(reinterpret_cast<void**>(&m->pent_blk), U * 4);
@@ -669,7 +720,8 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->tile_unit_off);
   cudaFree(m->unit_blk);
   cudaFree(m->unit_tile);
-  cudaFree(m->grp_unit);
+  cudaFree(m->grp_mp);
+  cudaFree(m->grp_ent);
   cudaFree(m->grp_cnt);
   cudaFree(m->ptile_off);
   cudaFree(m->pent_blk);
