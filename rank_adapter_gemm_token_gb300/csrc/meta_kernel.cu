@@ -13,6 +13,7 @@
 // rank inside its bin is (pairs of the same bin in earlier chunks) + (in earlier warps of
 // this chunk) + (in earlier lanes of its warp, from __match_any_sync). The result is
 // exactly the stable order; it does not depend on thread timing.
+#include <algorithm>
 #include <climits>
 
 #include "internal.h"
@@ -57,48 +58,58 @@ __device__ __forceinline__ void block_exclusive_scan3(int a, int b, int c, int& 
   __syncthreads();
 }
 
-// Exclusive prefix of per-lane counts over the warp; returns the exclusive prefix and sets *total.
-__device__ __forceinline__ int warp_exclusive(int c, int* total) {
-  const int lane = threadIdx.x & 31;
-  int inc = c;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc += t;
-  }
-  *total = __shfl_sync(0xffffffffu, inc, 31);
-  return inc - c;
-}
-
-// Bitmap (n_words words) of the column blocks owned by the slots of M-tile `tile`'s active pairs;
-// one warp. slot_blk[s] holds the first block of slot s in its low 16 bits and the last in its
-// high 16 bits (a slot of width w at column offset off covers blocks off / 64 .. (off + w - 1) / 64).
+// Bitmap (n_words words) of the column blocks owned by the slots of M-tile `tile`'s active pairs,
+// built by one warp without atomics. slot_blk[s] holds the first block of slot s in its low 16
+// bits and the last in its high 16 bits (a slot of width w at column offset off covers blocks
+// off / 64 .. (off + w - 1) / 64). Per round of 32 pairs and per block of their slots, the lanes
+// OR their bits word by word (one warp reduction per distinct word in the round).
 __device__ __forceinline__ void tile_block_bitmap(uint32_t* bm, int n_words, int tile, int T, int J,
                                                   const int* pslot, const uint32_t* slot_blk) {
   const int lane = threadIdx.x & 31;
   for (int k = lane; k < n_words; k += 32) bm[k] = 0u;
   __syncwarp();
-  // pairs of one slot share their blocks: per round of 32 pairs one lane per distinct slot sets
-  // the bits, and only bits not yet set cost an atomic (the words are few and heavily shared)
   const int p0 = tile * 128 * J, p1 = min(T, tile * 128 + 128) * J;
   for (int pb = p0; pb < p1; pb += 32) {
     const int p = pb + lane;
     const int s = p < p1 ? pslot[p] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, s);
-    if (s >= 0 && lane == __ffs(peers) - 1) {
-      const uint32_t sb = slot_blk[s];
-      for (int b = static_cast<int>(sb & 0xFFFFu); b <= static_cast<int>(sb >> 16); ++b) {
-        const uint32_t bit = 1u << (b & 31);
-        if (!(bm[b >> 5] & bit)) atomicOr(&bm[b >> 5], bit);
+    const uint32_t sb = s >= 0 ? slot_blk[s] : 0u;
+    const int b0 = static_cast<int>(sb & 0xFFFFu);
+    const int nblk = s >= 0 ? static_cast<int>(sb >> 16) - b0 + 1 : 0;
+    int more = __reduce_max_sync(0xffffffffu, nblk);
+    for (int i = 0; i < more; ++i) {
+      const bool has = i < nblk;
+      const int b = b0 + i;
+      const uint32_t w = has ? static_cast<uint32_t>(b >> 5) : 0xFFFFFFFFu;
+      unsigned todo = __ballot_sync(0xffffffffu, has);
+      while (todo) {
+        const uint32_t ww = __shfl_sync(0xffffffffu, w, __ffs(todo) - 1);
+        const bool mine = has && w == ww;
+        const uint32_t bits = __reduce_or_sync(0xffffffffu, mine ? (1u << (b & 31)) : 0u);
+        todo &= ~__ballot_sync(0xffffffffu, mine);
+        if (lane == 0) bm[ww] |= bits;
       }
     }
   }
   __syncwarp();
 }
 
+// Writes the positions of the set bits of a warp's bitmap in ascending order: bit b of the map
+// goes to out[base + rank of b]; one word per step, the lanes taking its 32 bits.
+template <typename F>
+__device__ __forceinline__ void emit_bits(const uint32_t* bm, int n_words, F&& put) {
+  const int lane = threadIdx.x & 31;
+  int run = 0;
+  for (int k = 0; k < n_words; ++k) {
+    const uint32_t w = bm[k];
+    if (w == 0u) continue;                               // uniform: every lane reads the same word
+    if ((w >> lane) & 1u) put(k * 32 + lane, run + __popc(w & ((1u << lane) - 1u)));
+    run += __popc(w);
+  }
+}
+
 __global__ void __launch_bounds__(kMetaThreads, 1)
 build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, PoolView pool,
-                  MetaView m, int cache) {
+                  MetaView m, int cache, int keep) {
   extern __shared__ int smem[];
   const int S = pool.S;
   const int nb = S + 1;
@@ -109,10 +120,12 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(actidx + nb);   // [32][nb]
   const int n_blocks = (pool.C + kBlockCols - 1) / kBlockCols;  // column blocks of the slot space
   const int n_words = (n_blocks + 31) / 32;
-  // after the sort the bins' area holds two block bitmaps per warp (the host sized it for both)
+  // after the sort the bins' area holds block bitmaps: with `keep`, one per M-tile, built once and
+  // read by every later step; otherwise two per warp, rebuilt where needed (the host sized it)
   uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem);
   const size_t bins_bytes = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
-  const size_t bm_bytes = static_cast<size_t>(32) * 2 * n_words * sizeof(uint32_t);
+  const int n_tiles_all = (m.T + 127) / 128;
+  const size_t bm_bytes = (keep ? static_cast<size_t>(n_tiles_all) : static_cast<size_t>(32) * 2) * n_words * sizeof(uint32_t);
   const size_t front = ((bins_bytes > bm_bytes ? bins_bytes : bm_bytes) + 15) / 16 * 16;
   uint32_t* slot_blk = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(smem) + front);   // [S]
   // small steps keep their pair slots, order and pair-blocks in shared memory as well, so the
@@ -252,12 +265,18 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   //    pairs' slots own (warp per tile, bitmap over the blocks), counted, capped, numbered.
   const int n_tiles = (m.T + 127) / 128;
   const int n_ptiles = (n_tiles + 1) / 2;
-  uint32_t* bmA = bitmaps + warp * 2 * n_words;
-  uint32_t* bmB = bmA + n_words;
+  uint32_t* scratchA = bitmaps + warp * 2 * n_words;     // without `keep`
+  uint32_t* scratchB = scratchA + n_words;
+  auto tile_map = [&](int i, uint32_t* scratch) -> const uint32_t* {
+    if (keep) return bitmaps + static_cast<size_t>(i) * n_words;
+    tile_block_bitmap(scratch, n_words, i, m.T, m.J, pslot, slot_blk);
+    return scratch;
+  };
   for (int i = warp; i < n_tiles; i += 32) {
-    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, slot_blk);
+    uint32_t* bm = keep ? bitmaps + static_cast<size_t>(i) * n_words : scratchA;
+    tile_block_bitmap(bm, n_words, i, m.T, m.J, pslot, slot_blk);
     int c = 0;
-    for (int w = lane; w < n_words; w += 32) c += __popc(bmA[w]);
+    for (int w = lane; w < n_words; w += 32) c += __popc(bm[w]);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
     if (lane == 0) tile_cnt[i] = c;
@@ -295,33 +314,21 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   __syncthreads();
   // units in ascending block order per tile
   for (int i = warp; i < n_tiles; i += 32) {
-    const int cnt = tile_cnt[i];
-    if (cnt == 0) continue;
-    tile_block_bitmap(bmA, n_words, i, m.T, m.J, pslot, slot_blk);
+    if (tile_cnt[i] == 0) continue;
+    const uint32_t* bm = tile_map(i, scratchA);
     const int ubase = tile_off[i];
-    int run = 0;
-    for (int k0 = 0; k0 < n_words; k0 += 32) {
-      const int kw = k0 + lane;
-      uint32_t w = kw < n_words ? bmA[kw] : 0u;
-      int total;
-      int pos = run + warp_exclusive(__popc(w), &total);
-      while (w) {
-        const int bit = __ffs(w) - 1;
-        w &= w - 1u;
-        m.unit_blk[ubase + pos] = kw * 32 + bit;
-        m.unit_tile[ubase + pos] = i;
-        ++pos;
-      }
-      run += total;
-    }
+    emit_bits(bm, n_words, [&](int b, int r) {
+      m.unit_blk[ubase + r] = b;
+      m.unit_tile[ubase + r] = i;
+    });
   }
   // pair tiles (M-tiles 2 mp and 2 mp + 1): the union of both tiles' blocks, each entry with the
   // unit of either tile on that block (-1 where the tile does not use it)
   for (int mp = warp; mp < n_ptiles; mp += 32) {
     const int ta = 2 * mp, tb = 2 * mp + 1;
     const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
-    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, slot_blk);
-    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, slot_blk);
+    const uint32_t* bmA = ha ? tile_map(ta, scratchA) : nullptr;
+    const uint32_t* bmB = hb ? tile_map(tb, scratchB) : nullptr;
     int c = 0;
     for (int w = lane; w < n_words; w += 32) c += __popc((ha ? bmA[w] : 0u) | (hb ? bmB[w] : 0u));
 #pragma unroll
@@ -354,31 +361,23 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     const int ta = 2 * mp, tb = 2 * mp + 1;
     const bool ha = tile_cnt[ta] > 0, hb = tb < n_tiles && tile_cnt[tb] > 0;
     if (!ha && !hb) continue;
-    if (ha) tile_block_bitmap(bmA, n_words, ta, m.T, m.J, pslot, slot_blk);
-    if (hb) tile_block_bitmap(bmB, n_words, tb, m.T, m.J, pslot, slot_blk);
-    int ra = 0, rb = 0, ru = 0;
+    const uint32_t* bmA = ha ? tile_map(ta, scratchA) : nullptr;
+    const uint32_t* bmB = hb ? tile_map(tb, scratchB) : nullptr;
     const int ua = tile_off[ta], ub = hb ? tile_off[tb] : 0, ebase = ptile_cnt[mp];
-    for (int k0 = 0; k0 < n_words; k0 += 32) {
-      const int kw = k0 + lane;
-      const uint32_t wa = (ha && kw < n_words) ? bmA[kw] : 0u, wb = (hb && kw < n_words) ? bmB[kw] : 0u;
-      uint32_t wu = wa | wb;
-      int ta_tot, tb_tot, tu_tot;
-      const int pa = ra + warp_exclusive(__popc(wa), &ta_tot);
-      const int pb = rb + warp_exclusive(__popc(wb), &tb_tot);
-      const int pu = ru + warp_exclusive(__popc(wu), &tu_tot);
-      const uint32_t all = wu;
-      while (wu) {
-        const int bit = __ffs(wu) - 1;
-        wu &= wu - 1u;
-        const uint32_t below = (1u << bit) - 1u;
-        const int e = ebase + pu + __popc(all & below);
-        m.pent_blk[e] = kw * 32 + bit;
-        m.pent_u0[e] = (wa >> bit) & 1u ? ua + pa + __popc(wa & below) : -1;
-        m.pent_u1[e] = (wb >> bit) & 1u ? ub + pb + __popc(wb & below) : -1;
+    int ra = 0, rb = 0, ru = 0;                          // set bits of earlier words
+    for (int k = 0; k < n_words; ++k) {
+      const uint32_t wa = ha ? bmA[k] : 0u, wb = hb ? bmB[k] : 0u, wu = wa | wb;
+      if (wu == 0u) continue;                              // uniform across the warp
+      if ((wu >> lane) & 1u) {
+        const uint32_t below = (1u << lane) - 1u;
+        const int e = ebase + ru + __popc(wu & below);
+        m.pent_blk[e] = k * 32 + lane;
+        m.pent_u0[e] = (wa >> lane) & 1u ? ua + ra + __popc(wa & below) : -1;
+        m.pent_u1[e] = (wb >> lane) & 1u ? ub + rb + __popc(wb & below) : -1;
       }
-      ra += ta_tot;
-      rb += tb_tot;
-      ru += tu_tot;
+      ra += __popc(wa);
+      rb += __popc(wb);
+      ru += __popc(wu);
     }
   }
   for (int p = tid; p < n; p += kMetaThreads) m.pair_fused[p] = pslot[p] >= 0 && !tile_ovf[(p / m.J) >> 7];
@@ -418,8 +417,14 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
   const int n = T * J;
   const size_t bins = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
   const size_t n_words = (static_cast<size_t>(pool.C) + kBlockCols * 32 - 1) / (kBlockCols * 32);
-  const size_t bitmaps = 32 * 2 * n_words * sizeof(uint32_t);
-  const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16 + (static_cast<size_t>(pool.S) * 4 + 15) / 16 * 16;
+  const size_t n_tiles = (static_cast<size_t>(T) + 127) / 128;
+  const size_t slots_bytes = (static_cast<size_t>(pool.S) * 4 + 15) / 16 * 16;
+  // keep every tile's bitmap when they fit beside the rest, else two scratch bitmaps per warp
+  const size_t kept = n_tiles * n_words * sizeof(uint32_t);
+  const size_t scratch = 32 * 2 * n_words * sizeof(uint32_t);
+  const int keep = ((std::max(bins, kept) + 15) / 16 * 16 + slots_bytes <= kMetaMaxDynSmem) ? 1 : 0;
+  const size_t bitmaps = keep ? kept : scratch;
+  const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16 + slots_bytes;
   if (front > kMetaMaxDynSmem) return cudaErrorInvalidValue;
   const int cache = front + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
   const size_t smem = front + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);
@@ -433,7 +438,7 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
     configured_device = dev;
   }
   note_launch_begin(kKindMeta, s);
-  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, pool, m, cache);
+  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, pool, m, cache, keep);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindMeta, s);
   return e;
