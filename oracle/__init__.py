@@ -8,11 +8,13 @@ and nothing here imports the library. The two share no code.
 - ``linear_sliced``: a fused linear whose output slices each have their own adapter.
 - ``meta``: the per-step slot metadata (stable sort of token/slot pairs by slot).
 - ``memory``: the adapter/slot memory arithmetic from the pages.
+- ``embedding``: the token embedding lookup with LoRA (``embed.py``, numpy fp64).
 
 Parity pins (tests/test_oracle.py) tie each function to the pages: a hand-worked
 example, the merge identity, the PEFT "cat" merge, linearity in the scale, the
 sentinel rows, the printed segment counts and the printed memory figures; the sliced
-form against the block-diagonal single-adapter identity.
+form against the block-diagonal single-adapter identity. The embedding lookup has its own
+pins (tests/test_oracle_embedding.py), among them its identity with ``linear`` on one-hot inputs.
 """
 from __future__ import annotations
 
@@ -154,3 +156,6 @@ def linear_sliced(x, W, token_slots, adapters, n_slots: int, widths, scales=None
         off += w
     assert off == W.shape[0]
     return np.concatenate(out, axis=1)
+
+
+from .embed import embedding  # noqa: E402,F401  (re-export; needs OracleError above)
