@@ -6,7 +6,8 @@ Workload (default): the mixed serving step -- a Llama-style stack of 32 layers x
 each), tenants Zipf(1.1) over 1000 registered adapters of ranks 8/16/64 admitted into 128 GPU
 slots. One step = build the slot metadata once, then every linear (base GEMM + shrink +
 expand). Metric: tokens per second through the step. Other workloads (decode, prefill,
-compose, logits, tiny) are behind --workload.
+compose, logits, tiny, and the embedding lookup with LoRA on the mixed step's tokens) are
+behind --workload.
 
 Output: one JSON line (rank 0). Kernel durations for the roofline come from a second pass of
 the same steps with per-kernel CUDA events (the library's trace), so that the events do not
@@ -41,7 +42,7 @@ sys.path.insert(0, ROOT)
 METRIC = "LoRA-linear tokens/s (1×GB300) + % of HBM / bf16 tensor roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-WORKLOADS = ("mixed", "decode", "compose", "prefill", "tiny", "logits")
+WORKLOADS = ("mixed", "decode", "compose", "prefill", "tiny", "logits", "embedding")
 
 
 def load_peaks():
@@ -89,11 +90,21 @@ def make_workload(name: str, layers: int = 32):
     import synth
     if name == "mixed":
         return synth.mixed(n_layers=layers)
+    if name == "embedding":
+        return synth.embedding_step()
     return {"decode": synth.decode, "logits": synth.logits, "compose": synth.compose, "tiny": synth.tiny,
             "prefill": synth.prefill}[name]()
 
 
 def workload_config(wl, name: str) -> dict:
+    if name == "embedding":
+        return {
+            "workload": f"embedding: {wl.T} tokens of the mixed step through a {wl.vocab} x {wl.dim} table with LoRA, "
+                        f"J={wl.J}, {wl.n_slots} slots in rank classes {wl.classes}",
+            "tokens_per_step": wl.T, "vocab": wl.vocab, "dim": wl.dim, "slots": wl.n_slots, "r_max": wl.r_max,
+            "slots_per_token": wl.J,
+            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+        }
     lin = wl.linears
     if len(lin) <= 8:
         what = ", ".join(f"{l.name} {l.K}->{l.D}" for l in lin)
@@ -175,6 +186,19 @@ def algorithmic(wl, num_sms: int = 152) -> dict:
             flops["base_gemm"] += f_base + f_expand
     out["flops"] = flops
     return out
+
+
+def algorithmic_embedding(wl) -> dict:
+    """Bytes and flops of the embedding lookup with LoRA per step: each token's table row (bf16)
+    and its fp32 output row, the ids, the token's A column of every active pair (r bf16 values),
+    B of every adapter in use once (at its true rank); flops 2 r D per active pair. The metadata
+    build: 24 bytes per pair."""
+    slots = wl.token_slots
+    active = slots >= 0
+    distinct = sorted(set(int(s) for s in slots[active]))
+    pair_r = int(sum(wl.adapters[int(s)].rank for s in slots[active]))
+    emb = wl.T * wl.dim * (2 + 4) + wl.T * 4 + pair_r * 2 + sum(wl.adapters[s].rank for s in distinct) * wl.dim * 2
+    return {"meta": wl.T * wl.J * 4 * 6, "embedding": emb, "flops": {"embedding": 2 * pair_r * wl.dim}}
 
 
 def roofline_of(byts: float, flops: float, seconds: float, peaks: dict) -> dict:
@@ -302,7 +326,29 @@ def oracle_sample(wl, budget_s: float = 12.0, max_rows: int | None = None):
     return rows_n / last, rows_n, threads, last, lazy
 
 
+def oracle_sample_embedding(wl, budget_s: float = 12.0, max_rows: int | None = None):
+    """The embedding oracle on a growing sample of token rows until about budget_s of CPU work;
+    returns (tokens/s, rows, threads, seconds for those rows, extrapolated=False)."""
+    import oracle
+    cap = wl.T if max_rows is None else min(wl.T, max_rows)
+    rows_n, spent = min(cap, 16), 0.0
+    rng = np.random.default_rng(0)
+    while True:
+        rows = np.sort(rng.choice(wl.T, size=rows_n, replace=False))
+        t0 = time.perf_counter()
+        oracle.embedding(wl.ids, wl.E, wl.token_slots, wl.adapters, wl.n_slots, scales=wl.scales, rows=rows)
+        real = time.perf_counter() - t0
+        spent += real
+        if rows_n >= cap or spent + real * 2.5 > budget_s:
+            break
+        rows_n = min(cap, rows_n * 2)
+    return rows_n / real, rows_n, 1, real, False
+
+
 def sample_note(wl, rows, seconds=None, lazy=False) -> str:
+    if not hasattr(wl, "linears"):
+        return f"{rows} of {wl.T} token rows through the embedding oracle" + (
+            f" ({seconds:.2f} s per step)" if seconds is not None else " per step")
     import synth
     what = (f"{rows} of {wl.T} token rows through the first {len(synth.MIXED_MODULES)} of {len(wl.linears)} "
             f"linears, time extrapolated to all of them" if lazy else
@@ -322,8 +368,9 @@ def run_reference(args):
     times = []
     lazy = False
     threads = 1
+    sampler = oracle_sample_embedding if args.workload == "embedding" else oracle_sample
     for i in range(args.warmup + args.steps):
-        _, rows, threads, dt, lazy = oracle_sample(wl, budget_s=step_budget, max_rows=rows)
+        _, rows, threads, dt, lazy = sampler(wl, budget_s=step_budget, max_rows=rows)
         if i >= args.warmup:
             times.append(dt)
     ms = 1000.0 * float(np.mean(times))
@@ -674,6 +721,166 @@ def run_ours(args):
     return 0
 
 
+def run_embedding(args):
+    """The embedding lookup with LoRA on the mixed step's tokens: one step = the metadata build and
+    one mlora_embedding call, captured as a graph and replayed; the same JSON line as the linear
+    workloads (roofline of the dominant kernel, step roofline, e2e with host buffers, oracle
+    baseline on a row sample)."""
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from rank_adapter_gemm_token_gb300 import layer, mlora
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+
+    t_setup = time.perf_counter()
+    wl = make_workload("embedding")
+    pool = layer.EmbeddingPool(wl.vocab, wl.dim, wl.classes)
+    for s_, ad in wl.adapters.items():
+        pool.load(s_, ad.A, ad.B, ad.rank, ad.alpha, ad.rslora)
+    pool.sync()
+    E = layer.bf16_from_bits(wl.E, device)
+    ids = torch.from_numpy(wl.ids.astype(np.int32)).to(device)
+    slots = torch.from_numpy(np.ascontiguousarray(wl.token_slots.astype(np.int32))).to(device)
+    meta = layer.StepMeta(wl.T, wl.J, wl.r_max)
+    y = torch.empty((wl.T, wl.dim), dtype=torch.float32, device=device)
+    torch.cuda.synchronize(device)
+    setup_s = time.perf_counter() - t_setup
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def step(s=None):
+        meta.build(slots, None, pool, s)
+        layer.embedding(pool, meta, ids, E, y, s)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(stream)
+    meta.status()
+    barrier()
+    l0 = mlora.mlora_launch_count()
+    step(stream)
+    kernels_per_step = mlora.mlora_launch_count() - l0
+    barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    wall0 = time.perf_counter()
+    ms_local, _ = time_graph(lambda: step(), args.steps, args.warmup, stream, flush, device, barrier)
+    wall = time.perf_counter() - wall0
+    clock_info = clocks.stop()
+    head = headline_fields(ms_local, wl.T)
+
+    trace_steps = min(args.steps, 20)
+    mlora.mlora_trace_enable(int(kernels_per_step) * trace_steps + 64)
+    for _ in range(trace_steps):
+        flush.zero_()
+        step(stream)
+    barrier()
+    trace = mlora.mlora_trace_read()
+    mlora.mlora_trace_disable()
+
+    # end to end: ids and token slots up from pinned host memory, the step, y down
+    ids_h, slots_h = ids.cpu().pin_memory(), slots.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e_step():
+        ids.copy_(ids_h, non_blocking=True)
+        slots.copy_(slots_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        e2e_step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 20))):
+        flush.zero_()
+        e_start.record(stream)
+        graph.replay()
+        e_end.record(stream)
+        e_end.synchronize()
+        e2e_ms.append(e_start.elapsed_time(e_end))
+    _, e2e_value = aggregate_over_ranks(float(np.mean(e2e_ms)), wl.T)
+    meta.status()
+    h2d, d2h = ids_h.numel() * 4 + slots_h.numel() * 4, y_h.numel() * 4
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    algo = algorithmic_embedding(wl)
+    kinds = {k: v for k, v in trace.items() if v[0] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][1])
+    n_launch, tot_ms = kinds[dom]
+    avg_s = tot_ms / n_launch / 1000.0
+    per_step = n_launch / trace_steps
+    rf = roofline_of(algo.get(dom, 0) / per_step, algo["flops"].get(dom, 0) / per_step, avg_s, peaks)
+    roofline = {"kernel": dom, "bound": rf["bound"], "achieved": rf["achieved"], "peak": rf["peak"],
+                "unit": rf["unit"], "frac": rf["frac"],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
+                "traffic": recorded_traffic(dom, "embedding"),
+                "algorithmic_bytes_per_launch": algo.get(dom, 0) / per_step,
+                "algorithmic_flops_per_launch": algo["flops"].get(dom, 0) / per_step,
+                "avg_launch_us": avg_s * 1e6}
+    total_traced = sum(v[1] for v in kinds.values())
+    per_kernel = {k: {"launches_per_step": n / trace_steps, "avg_us": 1000.0 * t / n, "share": t / total_traced}
+                  for k, (n, t) in kinds.items()}
+    step_bytes = sum(v for k, v in algo.items() if k != "flops")
+    srf = roofline_of(step_bytes, sum(algo["flops"].values()), ms_local / 1000.0, peaks)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        tps, rows, threads, dt, _ = oracle_sample_embedding(wl, budget_s=args.cpu_budget)
+        cpu = {"value": tps, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample_note(wl, rows, dt),
+               "extrapolated": False}
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": head["n_gpus"], "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": head["scaling"], "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox4x64-10 + Box-Muller, bf16-rounded)",
+        "config": dict(workload_config(wl, "embedding"), parallelism=head["parallelism"]),
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(kernels_per_step * args.steps), "clocks": clock_info, "kernels": per_kernel,
+        "step_roofline": {"bound": srf["bound"], "bound_us": srf["bound_us"],
+                          "frac": srf["bound_us"] / (ms_local * 1000.0), "hbm_frac": srf["hbm_frac"],
+                          "bytes_per_step": step_bytes},
+        "setup_s": setup_s, "wall_s_timed_region": wall,
+        "kernel_timing": f"second pass of {trace_steps} steps with per-kernel CUDA events on the launch stream",
+        "step_launch": "CUDA graph replay of the captured step",
+    }
+    print(json.dumps(line), flush=True)
+    pool.close()
+    meta.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def _free_port() -> int:
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
@@ -707,6 +914,8 @@ def main(argv=None):
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch one rank per GPU")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "embedding":
+        return run_embedding(args)
     return run_ours(args)
 
 

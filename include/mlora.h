@@ -65,7 +65,8 @@ enum {
   MLORA_ERR_CUDA = 8,             /* a CUDA call failed (message has the CUDA error)         */
   MLORA_ERR_DEVICE_TIMEOUT = 9,   /* a kernel's bounded wait gave up (the GPU stays usable)  */
   MLORA_ERR_MISMATCH = 10,        /* pool and metadata or pool and operands do not fit     */
-  MLORA_ERR_NO_FREE_SLOT = 11     /* a step needs more adapters resident than slots allow  */
+  MLORA_ERR_NO_FREE_SLOT = 11,    /* a step needs more adapters resident than slots allow  */
+  MLORA_ERR_BAD_TOKEN_ID = 12     /* a token id outside [0, vocab) of an embedding table     */
 };
 
 /* Limits of this build. */
@@ -274,6 +275,37 @@ MLORA_API mlora_status mlora_lora_apply_noalloc(const mlora_bf16* x, float* y, c
                                                 const int32_t* slot_rank, int n_slots, int r_pad, int K, int D,
                                                 void* stream);
 
+/* ------------------------------------------------------------------ embedding lookup -- */
+
+/* The slot pool of an embedding table with LoRA ("[vLLM] LoRA" (secrett2633 blog), layer
+ * implementation section: the embedding is one of the LoRA layer variants; "LoRA Serving" (vLLM
+ * learning book ch. 09-04), section 2). The lookup of token id i is the linear map of the one-hot
+ * vector e_i with weight E^T, so an adapter with A [r, vocab] and B [dim, r] adds c B A[:, i].
+ * Classes, slot numbering and the column space are those of mlora_pool_create_classes (one
+ * class: class_slots = {n_slots}, class_rank = {r_max}); A is kept token-major, A_pool
+ * [vocab, C] (row i holds column i of every slot's A), so a token's side path reads one
+ * contiguous run of its rank; B_pool is [dim, C]. vocab >= 1; dim a positive even number
+ * (else MLORA_ERR_INVALID_ARG). mlora_load_adapter, mlora_clear_slot, mlora_pool_sync,
+ * mlora_pool_layout and mlora_pool_info (K = vocab, D = dim) work on it as on a linear pool;
+ * A_host is the adapter's [rank, vocab] matrix, staged whole and written token-major by a
+ * kernel on the copy stream. mlora_load_adapter_sliced and the linear-layer calls
+ * (mlora_linear, mlora_lora_shrink, mlora_lora_expand) reject it with MLORA_ERR_INVALID_ARG. */
+MLORA_API mlora_status mlora_embedding_pool_create(int n_classes, const int* class_slots, const int* class_rank,
+                                                   int vocab, int dim, void* copy_stream, mlora_pool_t* out);
+
+/* Embedding lookup with LoRA for the step described by `meta` (built by mlora_build_meta with
+ * this pool or one of the same slots and classes):
+ *     y[t, :] = E[ids[t], :] + sum_{j : slot[t,j] != -1} s[t,j] c(slot) B_slot A_slot[:, ids[t]]
+ *   ids: device int32 [T] (T = the meta's last build); E: device bf16 [vocab, dim] row-major;
+ *   y: device fp32 [T, dim], overwritten (rows whose slots are all -1 equal the table row
+ *   exactly). E and y 16-byte aligned. A token id outside [0, vocab) gives a zero row and is
+ *   reported by mlora_meta_status as MLORA_ERR_BAD_TOKEN_ID. One kernel on the CUDA cores (the
+ *   lookup is bound by memory traffic); each output is a fixed sequence of fp32 operations.
+ * Orders itself after the pool's queued loads; calls sharing a meta or a pool must be ordered
+ * on one stream. */
+MLORA_API mlora_status mlora_embedding(mlora_pool_t pool, mlora_meta_t meta, const int32_t* ids, const mlora_bf16* E,
+                                       float* y, void* stream);
+
 /* ------------------------------------------------------------------ slot residency ---- */
 
 /* Which adapter id sits in which of n_slots GPU slots ("LoRA Serving", section 5: the LRU cache
@@ -337,7 +369,8 @@ MLORA_API mlora_status mlora_check_wait_timeout(void* stream);
 /* Per-kernel CUDA-event trace. While enabled, every kernel launch is bracketed by two events
  * on its own stream (at most `capacity` launches are kept). mlora_trace_read synchronises
  * and returns, for each kernel kind, the number of launches and their summed device time in
- * milliseconds; kinds: 0 meta, 1 base GEMM, 2 shrink, 3 expand, 4 slot bookkeeping. */
+ * milliseconds; kinds: 0 meta, 1 base GEMM, 2 shrink, 3 expand, 4 slot bookkeeping, 5 embedding
+ * lookup. */
 MLORA_API mlora_status mlora_trace_enable(int capacity);
 MLORA_API mlora_status mlora_trace_disable(void);
 MLORA_API mlora_status mlora_trace_read(int n_kinds, int* launches, double* total_ms);

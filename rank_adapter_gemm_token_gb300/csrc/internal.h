@@ -89,7 +89,9 @@ constexpr int kVfullMaxTokens = 256;
 constexpr int kVfullMaxAct = 512;
 
 // Kernel kinds for the launch counter and the optional per-kernel event trace.
-enum KernelKind : int { kKindMeta = 0, kKindGemm = 1, kKindShrink = 2, kKindExpand = 3, kKindSlot = 4, kNumKinds = 5 };
+enum KernelKind : int {
+  kKindMeta = 0, kKindGemm = 1, kKindShrink = 2, kKindExpand = 3, kKindSlot = 4, kKindEmbed = 5, kNumKinds = 6
+};
 
 // Records the thread's last-error message and returns the status (mlora_runtime.cu).
 int report_error(int status, const char* message);
@@ -160,5 +162,14 @@ cudaError_t launch_lora_shrink(const uint16_t* x, const PoolView& pool, const Me
                                cudaStream_t s, bool skip_fused = false);
 cudaError_t launch_lora_expand(float* y, const PoolView& pool, const MetaView& m, int num_sms, cudaStream_t s,
                                bool skip_fused = false);
+
+// Embedding lookup with LoRA (embedding.cu) over an embedding pool (A stored token-major as
+// A^T [V, C] in PoolView::A, V in PoolView::K): y[t] = E[ids[t]] + sum_j s c B A[:, ids[t]].
+cudaError_t launch_embedding(const int32_t* ids, const uint16_t* E, float* y, const PoolView& pool, const MetaView& m,
+                             int num_sms, cudaStream_t s);
+// Writes columns off .. off + width - 1 of A^T [V, C] from an adapter's A [r, V] staged whole
+// (zeros past the rank; r = 0 clears them).
+cudaError_t launch_scatter_slot_at(uint16_t* At, int C, int off, int width, int V, const uint16_t* stage, int r,
+                                   cudaStream_t s);
 
 }  // namespace mlora

@@ -174,14 +174,15 @@ struct mlora_pool {
   int device = 0;
   int S = 0, r_max = 0, R = 0, K = 0, D = 0;
   int C = 0;                                   // columns of the slot space
-  uint16_t* A = nullptr;                       // [C, K]
+  bool embed = false;                          // an embedding pool: A token-major, K = vocabulary
+  uint16_t* A = nullptr;                       // [C, K] ([K, C] for an embedding pool)
   uint16_t* B = nullptr;                       // [D, C]
   float* slot_scale = nullptr;
   int32_t* slot_rank = nullptr;
   int32_t* slot_off = nullptr;                 // [S] first column of each slot
   int32_t* slot_width = nullptr;               // [S] columns of each slot
   int32_t* col_slot = nullptr;                 // [C] slot owning each column
-  uint16_t* stage = nullptr;                   // [D * R] a loading adapter's B, before its scatter
+  uint16_t* stage = nullptr;                   // [D * R] a loading adapter's B (or embedding A), before its scatter
   std::vector<int> class_slots, class_rank;    // the rank classes (one for mlora_pool_create)
   std::vector<int> h_rank, h_off, h_width, h_class;
   int max_span = 1;                            // most 64-column blocks one slot touches
@@ -311,12 +312,13 @@ const char* mlora_status_string(mlora_status s) {
     case MLORA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
     case MLORA_ERR_MISMATCH: return "pool, metadata and operands do not fit together";
     case MLORA_ERR_NO_FREE_SLOT: return "more adapters needed at once than free or evictable slots";
+    case MLORA_ERR_BAD_TOKEN_ID: return "a token id outside the embedding table";
     default: return "unknown status";
   }
 }
 
 const char* mlora_kernel_kind_name(int kind) {
-  static const char* names[kNumKinds] = {"meta", "base_gemm", "shrink", "expand", "slot"};
+  static const char* names[kNumKinds] = {"meta", "base_gemm", "shrink", "expand", "slot", "embedding"};
   return (kind >= 0 && kind < kNumKinds) ? names[kind] : "?";
 }
 
@@ -332,7 +334,7 @@ size_t mlora_pool_bytes(int n_slots, int r_max, int K, int D) {
 // straddles two 64-column blocks), so a pool's layout is a function of its class list alone and
 // pools created with the same classes lay out their slots identically.
 static mlora_status pool_create(int n_classes, const int* class_slots, const int* class_rank, int K, int D,
-                                void* copy_stream, mlora_pool_t* out) {
+                                void* copy_stream, mlora_pool_t* out, bool embed = false) {
   if (!out) return fail(MLORA_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (n_classes < 1 || n_classes > MLORA_MAX_CLASSES || !class_slots || !class_rank)
@@ -348,13 +350,19 @@ static mlora_status pool_create(int n_classes, const int* class_slots, const int
     r_max = std::max(r_max, class_rank[c]);
   }
   if (S > MLORA_MAX_SLOTS) return fail(MLORA_ERR_INVALID_ARG, "%ld slots: more than %d", S, MLORA_MAX_SLOTS);
-  if (K < 8 || K % 8 != 0) return fail(MLORA_ERR_INVALID_ARG, "K %d must be a positive multiple of 8", K);
-  if (D < 1) return fail(MLORA_ERR_INVALID_ARG, "D %d must be positive", D);
+  if (embed) {
+    if (K < 1) return fail(MLORA_ERR_INVALID_ARG, "vocabulary %d must be positive", K);
+    if (D < 2 || D % 2 != 0) return fail(MLORA_ERR_INVALID_ARG, "embedding width %d must be a positive even number", D);
+  } else {
+    if (K < 8 || K % 8 != 0) return fail(MLORA_ERR_INVALID_ARG, "K %d must be a positive multiple of 8", K);
+    if (D < 1) return fail(MLORA_ERR_INVALID_ARG, "D %d must be positive", D);
+  }
   DeviceState* ds = nullptr;
   if (mlora_status st = device_state(&ds)) return st;
   mlora_pool* p = new (std::nothrow) mlora_pool();
   if (!p) return fail(MLORA_ERR_OOM, "host allocation failed");
   cudaGetDevice(&p->device);
+  p->embed = embed;
   p->S = static_cast<int>(S);
   p->r_max = r_max;
   p->R = slot_width(r_max);
@@ -389,7 +397,7 @@ static mlora_status pool_create(int n_classes, const int* class_slots, const int
       (e = cudaMalloc(&p->slot_off, p->S * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->slot_width, p->S * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->col_slot, p->C * sizeof(int32_t))) != cudaSuccess ||
-      (e = cudaMalloc(&p->stage, static_cast<size_t>(D) * p->R * 2)) != cudaSuccess) {
+      (e = cudaMalloc(&p->stage, static_cast<size_t>(embed ? std::max(D, K) : D) * p->R * 2)) != cudaSuccess) {
     cudaGetLastError();
     mlora_pool_destroy(p);
     return e == cudaErrorMemoryAllocation ? fail(MLORA_ERR_OOM, "cudaMalloc of %zu + %zu bytes failed", a_bytes, b_bytes)
@@ -441,6 +449,11 @@ mlora_status mlora_pool_create_classes(int n_classes, const int* class_slots, co
   return pool_create(n_classes, class_slots, class_rank, K, D, copy_stream, out);
 }
 
+mlora_status mlora_embedding_pool_create(int n_classes, const int* class_slots, const int* class_rank, int vocab,
+                                         int dim, void* copy_stream, mlora_pool_t* out) {
+  return pool_create(n_classes, class_slots, class_rank, vocab, dim, copy_stream, out, true);
+}
+
 mlora_status mlora_pool_layout(mlora_pool_t p, int* C, int32_t* slot_off, int32_t* slot_width) {
   if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
   if (C) *C = p->C;
@@ -488,16 +501,17 @@ static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, co
   const size_t off = static_cast<size_t>(p->h_off[slot]);
   const size_t width = static_cast<size_t>(p->h_width[slot]);
   uint16_t* a_slot = p->A + off * p->K;
-  MLORA_CUDA(cudaMemsetAsync(a_slot, 0, width * p->K * 2, cs), "zero slot A");
+  if (!p->embed) MLORA_CUDA(cudaMemsetAsync(a_slot, 0, width * p->K * 2, cs), "zero slot A");
   SliceRows sl{};
   sl.n = n_slices;
   int row = 0;
   for (int i = 0; i < n_slices; ++i) {
     const int w = widths ? widths[i] : p->D;
     sl.row0[i] = row;
-    MLORA_CUDA(cudaMemcpyAsync(a_slot + static_cast<size_t>(i) * r * p->K, A_host[i], static_cast<size_t>(r) * p->K * 2,
-                               cudaMemcpyHostToDevice, cs),
-               "copy A into slot");
+    if (!p->embed)
+      MLORA_CUDA(cudaMemcpyAsync(a_slot + static_cast<size_t>(i) * r * p->K, A_host[i],
+                                 static_cast<size_t>(r) * p->K * 2, cudaMemcpyHostToDevice, cs),
+                 "copy A into slot");
     MLORA_CUDA(cudaMemcpyAsync(p->stage + static_cast<size_t>(row) * r, B_host[i], static_cast<size_t>(w) * r * 2,
                                cudaMemcpyHostToDevice, cs),
                "copy B to the staging buffer");
@@ -513,6 +527,19 @@ static mlora_status write_slot_sliced(mlora_pool_t p, int slot, int n_slices, co
     cudaError_t e = cudaGetLastError();
     note_launch_end(kKindSlot, cs);
     if (e != cudaSuccess) return cuda_fail(e, "scatter_slot_b_kernel");
+  }
+  if (p->embed) {
+    // an embedding pool's A [r, V] is staged whole (after the B scatter, in stream order) and
+    // written token-major into columns off .. off + width - 1 of A^T [V, C]
+    const int ra = n_slices > 0 ? r : 0;
+    if (ra > 0)
+      MLORA_CUDA(cudaMemcpyAsync(p->stage, A_host[0], static_cast<size_t>(ra) * p->K * 2, cudaMemcpyHostToDevice, cs),
+                 "copy A to the staging buffer");
+    note_launch_begin(kKindSlot, cs);
+    cudaError_t e = launch_scatter_slot_at(p->A, p->C, static_cast<int>(off), static_cast<int>(width), p->K, p->stage,
+                                           ra, cs);
+    note_launch_end(kKindSlot, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter_slot_at_kernel");
   }
   const int rank = n_slices * r;
   note_launch_begin(kKindSlot, cs);
@@ -557,6 +584,7 @@ mlora_status mlora_load_adapter_sliced(mlora_pool_t p, int slot, int n_slices, c
   if (slot < 0 || slot >= p->S) return fail(MLORA_ERR_SLOT_RANGE, "slot %d outside [0, %d)", slot, p->S);
   if (n_slices < 1 || n_slices > MLORA_MAX_SLICES)
     return fail(MLORA_ERR_INVALID_ARG, "n_slices %d outside [1, %d]", n_slices, MLORA_MAX_SLICES);
+  if (p->embed) return fail(MLORA_ERR_INVALID_ARG, "an embedding pool takes whole adapters (mlora_load_adapter)");
   if (!widths || !A_slices || !B_slices) return fail(MLORA_ERR_INVALID_ARG, "widths or slice arrays are NULL");
   long total = 0;
   for (int i = 0; i < n_slices; ++i) {
@@ -785,6 +813,7 @@ mlora_status mlora_meta_status(mlora_meta_t m) {
     return fail(MLORA_ERR_BAD_TOKEN_SLOT, "pair %d (token %d, slot index %d) names an invalid or empty slot", p,
                 m->J > 0 ? p / m->J : p, m->J > 0 ? p % m->J : 0);
   }
+  if (err & ptx::kErrBadId) return fail(MLORA_ERR_BAD_TOKEN_ID, "a token id lies outside the embedding table");
   if ((err | gerr) & ptx::kErrShape) return fail(MLORA_ERR_INVALID_ARG, "a kernel saw unsupported sizes");
   return MLORA_OK;
 }
@@ -842,6 +871,7 @@ static mlora_status check_pair(mlora_pool_t p, mlora_meta_t m) {
 }
 
 mlora_status mlora_lora_shrink(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, void* stream) {
+  if (p && p->embed) return fail(MLORA_ERR_INVALID_ARG, "an embedding pool: use mlora_embedding");
   if (mlora_status st = check_pair(p, m)) return st;
   if (m->T > 0 && (!x || !aligned16(x))) return fail(MLORA_ERR_INVALID_ARG, "x is NULL or misaligned");
   DeviceState* ds = nullptr;
@@ -855,6 +885,7 @@ mlora_status mlora_lora_shrink(mlora_pool_t p, mlora_meta_t m, const mlora_bf16*
 }
 
 mlora_status mlora_lora_expand(mlora_pool_t p, mlora_meta_t m, float* y, void* stream) {
+  if (p && p->embed) return fail(MLORA_ERR_INVALID_ARG, "an embedding pool: use mlora_embedding");
   if (mlora_status st = check_pair(p, m)) return st;
   if (m->T > 0 && (!y || !aligned16(y))) return fail(MLORA_ERR_INVALID_ARG, "y is NULL or misaligned");
   DeviceState* ds = nullptr;
@@ -869,6 +900,7 @@ mlora_status mlora_lora_expand(mlora_pool_t p, mlora_meta_t m, float* y, void* s
 
 mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, const mlora_bf16* W, float* y,
                           void* stream) {
+  if (p && p->embed) return fail(MLORA_ERR_INVALID_ARG, "an embedding pool: use mlora_embedding");
   if (mlora_status st = check_pair(p, m)) return st;
   if (mlora_status st = check_operands(x, W, y, m->T, p->K, p->D)) return st;
   DeviceState* ds = nullptr;
@@ -914,6 +946,22 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
       if ((e = launch_lora_expand(y, pv, mv, ds->num_sms, s, true)) != cudaSuccess) return cuda_fail(e, "expand launch");
     }
   }
+  m->last_stream = s;
+  return MLORA_OK;
+}
+
+mlora_status mlora_embedding(mlora_pool_t p, mlora_meta_t m, const int32_t* ids, const mlora_bf16* E, float* y,
+                             void* stream) {
+  if (p && !p->embed) return fail(MLORA_ERR_INVALID_ARG, "not an embedding pool (mlora_embedding_pool_create)");
+  if (mlora_status st = check_pair(p, m)) return st;
+  if (m->T > 0 && (!ids || !E || !y)) return fail(MLORA_ERR_INVALID_ARG, "ids, E or y is NULL");
+  if ((E && !aligned16(E)) || (y && !aligned16(y))) return fail(MLORA_ERR_INVALID_ARG, "E and y must be 16-byte aligned");
+  DeviceState* ds = nullptr;
+  if (mlora_status st = device_state(&ds)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mlora_status st = pool_use(p, s)) return st;
+  cudaError_t e = launch_embedding(ids, E, y, p->view(), m->view(), ds->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "embedding launch");
   m->last_stream = s;
   return MLORA_OK;
 }

@@ -12,6 +12,7 @@ namespace ptx {
 constexpr uint32_t kErrWaitTimeout = 1u << 0;   // a bounded mbarrier wait gave up
 constexpr uint32_t kErrBadSlot = 1u << 1;       // a token named an invalid or empty slot
 constexpr uint32_t kErrShape = 1u << 2;         // a launch saw sizes it cannot handle
+constexpr uint32_t kErrBadId = 1u << 3;         // a token id outside the embedding table
 
 // A wait gives up after this many nanoseconds of %globaltimer (2 s): far above any
 // legitimate wait of these kernels, short enough to leave the GPU usable.

@@ -78,6 +78,21 @@ class AdapterPool:
             pass
 
 
+class EmbeddingPool(AdapterPool):
+    """The slots of an embedding table with LoRA: A kept token-major ([vocab, C]), B [dim, C].
+    load() takes each adapter's A [rank, vocab] and B [dim, rank], like a linear pool with
+    K = vocab and D = dim."""
+
+    def __init__(self, vocab: int, dim: int, classes, copy_stream=None):
+        self.K, self.D = vocab, dim
+        self.classes = [(int(n), int(r)) for n, r in classes]
+        self.n_slots = sum(n for n, _ in self.classes)
+        self.r_max = max(r for _, r in self.classes)
+        self.handle = mlora.mlora_embedding_pool_create([n for n, _ in self.classes], [r for _, r in self.classes],
+                                                        vocab, dim, copy_stream)
+        self._staged = []
+
+
 class StepMeta:
     """Per-step slot metadata for up to max_tokens tokens with J slots each."""
 
@@ -128,6 +143,18 @@ def linear(pool: AdapterPool, meta: StepMeta, x: torch.Tensor, W: torch.Tensor, 
     if y is None:
         y = torch.empty((T, pool.D), dtype=torch.float32, device=x.device)
     mlora.mlora_linear(pool.handle, meta.handle, x, W, y, _stream(stream))
+    return y
+
+
+def embedding(pool: EmbeddingPool, meta: StepMeta, ids: torch.Tensor, E: torch.Tensor, y: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """y[T, dim] fp32 = E[ids] + the step's LoRA side path (ids int32 [T], E [vocab, dim] bf16 on the GPU)."""
+    assert ids.dtype == torch.int32 and E.dtype == torch.bfloat16 and ids.is_contiguous() and E.is_contiguous()
+    T = meta.T
+    assert ids.shape == (T,) and E.shape == (pool.K, pool.D)
+    if y is None:
+        y = torch.empty((T, pool.D), dtype=torch.float32, device=E.device)
+    mlora.mlora_embedding(pool.handle, meta.handle, ids, E, y, _stream(stream))
     return y
 
 

@@ -26,8 +26,9 @@ MLORA_ERR_CUDA = 8
 MLORA_ERR_DEVICE_TIMEOUT = 9
 MLORA_ERR_MISMATCH = 10
 MLORA_ERR_NO_FREE_SLOT = 11
+MLORA_ERR_BAD_TOKEN_ID = 12
 
-KERNEL_KINDS = ("meta", "base_gemm", "shrink", "expand", "slot")
+KERNEL_KINDS = ("meta", "base_gemm", "shrink", "expand", "slot", "embedding")
 
 EXPORTS = (
     "mlora_pool_create", "mlora_pool_destroy", "mlora_load_adapter", "mlora_clear_slot", "mlora_pool_sync",
@@ -40,7 +41,7 @@ EXPORTS = (
     "mlora_slot_cache_lookup", "mlora_slot_cache_pin", "mlora_slot_cache_evict", "mlora_adapter_cache_create",
     "mlora_adapter_cache_destroy", "mlora_adapter_cache_register", "mlora_adapter_cache_unregister",
     "mlora_adapter_cache_pin", "mlora_adapter_cache_map", "mlora_pool_create_classes", "mlora_pool_layout",
-    "mlora_set_path",
+    "mlora_set_path", "mlora_embedding_pool_create", "mlora_embedding",
 )
 
 
@@ -74,6 +75,8 @@ def load(path: str | None = None):
             "mlora_pool_create_classes": [i32, vp, vp, i32, i32, vp, vp],
             "mlora_pool_layout": [vp, vp, vp, vp],
             "mlora_set_path": [i32],
+            "mlora_embedding_pool_create": [i32, vp, vp, i32, i32, vp, vp],
+            "mlora_embedding": [vp, vp, vp, vp, vp, vp],
             "mlora_pool_destroy": [vp],
             "mlora_load_adapter": [vp, i32, vp, vp, i32, f32, i32],
             "mlora_clear_slot": [vp, i32],
@@ -171,6 +174,19 @@ def mlora_pool_create_classes(class_slots, class_rank, K: int, D: int, copy_stre
     return out.value
 
 
+def mlora_embedding_pool_create(class_slots, class_rank, vocab: int, dim: int, copy_stream=None) -> int:
+    """The slot pool of an embedding table [vocab, dim]: class c has class_slots[c] slots of rank <= class_rank[c]."""
+    lib = load()
+    n = len(class_slots)
+    assert len(class_rank) == n
+    cs = (ctypes.c_int * n)(*[int(v) for v in class_slots])
+    cr = (ctypes.c_int * n)(*[int(v) for v in class_rank])
+    out = ctypes.c_void_p()
+    _check(lib.mlora_embedding_pool_create(n, cs, cr, vocab, dim, _stream(copy_stream), ctypes.byref(out)),
+           "mlora_embedding_pool_create")
+    return out.value
+
+
 def mlora_pool_layout(pool: int, n_slots: int) -> dict:
     """The pool's column space: C and each slot's first column and width."""
     c = ctypes.c_int()
@@ -264,6 +280,11 @@ def mlora_meta_read(meta: int, n_pairs: int) -> dict:
 # ------------------------------------------------------------------------- layer
 def mlora_linear(pool: int, meta: int, x, W, y, stream=None) -> None:
     _check(load().mlora_linear(pool, meta, _ptr(x), _ptr(W), _ptr(y), _stream(stream)), "mlora_linear")
+
+
+def mlora_embedding(pool: int, meta: int, ids, E, y, stream=None) -> None:
+    """y[t] = E[ids[t]] + the step's LoRA side path on the lookup (ids int32 [T], E bf16 [vocab, dim], y fp32 [T, dim])."""
+    _check(load().mlora_embedding(pool, meta, _ptr(ids), _ptr(E), _ptr(y), _stream(stream)), "mlora_embedding")
 
 
 def mlora_base_gemm(x, W, y, T: int, K: int, D: int, stream=None) -> None:

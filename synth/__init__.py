@@ -441,3 +441,99 @@ def linear_weight(wl: Workload, lin: Linear) -> np.ndarray:
         return lin.W
     l, m = _layer_module(wl, lin)
     return mixed_weight_rows(wl.seed, l, m, lin.K, 0, lin.D)
+
+
+# --------------------------------------------------------------------------------------
+# Embedding lookup with LoRA
+# --------------------------------------------------------------------------------------
+
+_NS_EMB = 8
+
+
+@dataclass
+class EmbeddingWorkload:
+    """Token ids through an embedding table with LoRA adapters in rank-class slots."""
+    name: str
+    seed: int
+    T: int
+    J: int
+    vocab: int
+    dim: int
+    ids: np.ndarray                 # [T] int32 in [0, vocab)
+    token_slots: np.ndarray         # [T, J] int32, -1 = no adapter
+    scales: np.ndarray | None       # [T, J] float32 or None (= 1)
+    E: np.ndarray                   # [vocab, dim] bf16 bits
+    adapters: dict                  # slot -> Adapter with A [rank, vocab], B [dim, rank]
+    classes: list                   # [(slots, rank), ...]
+
+    @property
+    def n_slots(self) -> int:
+        return sum(n for n, _ in self.classes)
+
+    @property
+    def r_max(self) -> int:
+        return max(r for _, r in self.classes)
+
+
+def _embedding_tensors(seed, vocab, dim, T):
+    ids = (raw_u64(seed, tensor_key(_NS_EMB, 0), T) % np.uint64(vocab)).astype(np.int32)
+    E = normal_bf16(seed, tensor_key(_NS_EMB, 1), (vocab, dim), 0.02)
+    return ids, E
+
+
+def _embedding_adapter(seed, adapter_id, vocab, dim, rank, alpha, rslora):
+    A = normal_bf16(seed, tensor_key(_NS_EMB, 2, adapter_id), (rank, vocab), 0.02)
+    B = normal_bf16(seed, tensor_key(_NS_EMB, 3, adapter_id), (dim, rank), 0.02)
+    return Adapter(A=A, B=B, rank=rank, alpha=float(alpha), rslora=bool(rslora))
+
+
+def embedding_step(vocab: int = 100000, dim: int = 4096) -> EmbeddingWorkload:
+    """The mixed serving step's batch through the token embedding: the same 1024 tokens and token
+    -> slot map (mixed_step_plan: 4 x 192 prefill + 256 decode tokens, 112 adapters admitted into
+    128 slots in rank classes 8 / 16 / 64, alpha = 2r), token ids uniform over the vocabulary
+    (100000 x 4096, the memory example's table), E ~ N(0, 0.02), A [r, vocab] and B [dim, r]
+    ~ N(0, 0.02) per adapter id."""
+    plan = mixed_step_plan()
+    seed = plan["seed"]
+    ids, E = _embedding_tensors(seed, vocab, dim, plan["T"])
+    adapters = {s: _embedding_adapter(seed, a, vocab, dim, plan["rank_of"][a], 2.0 * plan["rank_of"][a], False)
+                for a, s in plan["slot_of"].items()}
+    return EmbeddingWorkload("embedding", seed, plan["T"], 1, vocab, dim, ids, plan["token_slots"], None, E,
+                             adapters, plan["classes"])
+
+
+def embedding_case(T: int, vocab: int, dim: int, J: int, classes, sentinel_frac: float = 0.15,
+                   with_scales: bool = True, seed_offset: int = 20) -> EmbeddingWorkload:
+    """A small embedding workload for parity tests: every slot of the classes holds an adapter
+    (rank = its class's rank for the first slot of a class, else uniform in [1, class rank];
+    alpha = 2r; odd slots rsLoRA); each token draws n ~ U{1..J} distinct slots (trailing -1),
+    sentinel_frac of the tokens none; scales U[0.2, 1.0] or None."""
+    seed = SEED_BASE + seed_offset
+    n_slots = sum(n for n, _ in classes)
+    ids, E = _embedding_tensors(seed, vocab, dim, T)
+    rw = raw_u64(seed, tensor_key(_NS_EMB, 4), n_slots)
+    adapters, s = {}, 0
+    for n, r_cls in classes:
+        for i in range(n):
+            r = r_cls if i == 0 else 1 + int(rw[s] % np.uint64(r_cls))
+            adapters[s] = _embedding_adapter(seed, s, vocab, dim, r, 2.0 * r, s % 2 == 1)
+            s += 1
+    n_act = (raw_u64(seed, tensor_key(_NS_SLOTS, 0), T) % np.uint64(J)).astype(np.int64) + 1
+    none = uniform01(seed, tensor_key(_NS_SLOTS, 2), T) < sentinel_frac
+    words = raw_u64(seed, tensor_key(_NS_SLOTS, 1), T * J).reshape(T, J)
+    slots = np.full((T, J), -1, dtype=np.int32)
+    for t in range(T):
+        if none[t]:
+            continue
+        pool = list(range(n_slots))
+        for j in range(min(int(n_act[t]), n_slots)):     # partial Fisher-Yates, without replacement
+            k = j + int(words[t, j] % np.uint64(n_slots - j))
+            pool[j], pool[k] = pool[k], pool[j]
+            slots[t, j] = pool[j]
+    scales = None
+    if with_scales:
+        u = uniform01(seed, tensor_key(_NS_SCALES, 0), T * J).reshape(T, J)
+        scales = (0.2 + 0.8 * u).astype(np.float32)
+        scales[slots < 0] = 0.0
+    return EmbeddingWorkload("embedding_case", seed, T, J, vocab, dim, ids, slots, scales, E, adapters,
+                             [(int(n), int(r)) for n, r in classes])
