@@ -666,6 +666,12 @@ cudaError_t launch_base_gemm_lora(const uint16_t* x, const uint16_t* W, float* y
   return launch_tc<64, 8>(x, W, y, T, K, D, err, num_sms, pool, meta, s);
 }
 
+bool base_gemm_uses_pair(int T) {
+  const int forced_n = gemm_tile_n();
+  if (forced_n > 0) return true;
+  return forced_n == 0 && (T + BM - 1) / BM > 1 && pair_gemm_max_pairs() > 0;
+}
+
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,
                              uint32_t* err, int num_sms, cudaStream_t s) {
   return launch_base_gemm_lora(x, W, y, T, K, D, err, num_sms, nullptr, nullptr, s);

@@ -75,6 +75,10 @@ struct MetaView {
   int32_t* pent_blk;      // [U] column block of each pair-tile entry (ascending within a pair tile)
   int32_t* pent_u0;       // [U] unit of M-tile 2mp with that block (-1: none)
   int32_t* pent_u1;       // [U] unit of M-tile 2mp + 1 with that block (-1: none)
+  int32_t* ptile_order;   // [pair tiles] pair tiles by entry count, most first (ties ascending)
+  uint32_t* sync;         // [2 + pair tiles] the pair GEMM's counters: [0] next tile ticket, [1] clusters
+                          //   done, [2 + mp] shrink sub-tiles of pair tile mp written (one per epilogue
+                          //   warp); zero between launches (the last cluster of a launch resets them)
   int32_t* pair_fused;    // [n] 1: the pair's side path runs on the tensor cores inside the GEMM
   int32_t* todo_blk;      // [n] ascending pair-block numbers holding a pair with pair_fused == 0
   uint16_t* vtile;        // [U][128][64] bf16: s c v of the unit's tokens on the block's columns
@@ -150,6 +154,11 @@ cudaError_t launch_wait_check(uint32_t* err, cudaStream_t s);
 // launch_pair_gemm picks it. gemm_tile_n() is the process-wide choice set by
 // mlora_set_gemm_tile_n (0 automatic, -1 never the pair kernel, else that N tile).
 int pair_gemm_max_pairs();
+// Whether launch_base_gemm_lora takes the CTA-pair kernel for a batch of T tokens, and whether
+// that kernel then also computes the shrink of the tensor-core side path (as tiles of its own
+// schedule) for inputs of width K.
+bool base_gemm_uses_pair(int T);
+bool pair_gemm_fuses_shrink(int K);
 int pair_gemm_pick_n(int T, int D, int max_pairs);
 cudaError_t launch_pair_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                              const PoolView* pool, const MetaView* meta, int bn, cudaStream_t s);

@@ -354,6 +354,17 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
       m.grp_ent[goff + g] = off + g * kGroupUnits;
       m.grp_cnt[goff + g] = min(kGroupUnits, c - g * kGroupUnits);
     }
+    // the pair tiles with the most entries first (the pair GEMM hands out their tiles first)
+    if (tid < n_ptiles) {
+      int r = 0;
+      for (int q = 0; q < n_ptiles; ++q) {
+        const int cq = ptile_cnt[q];
+        r += (cq > c || (cq == c && q < tid)) ? 1 : 0;
+      }
+      m.ptile_order[r] = tid;
+    }
+    for (int i = tid; i < n_ptiles + 2; i += kMetaThreads) m.sync[i] = 0u;
+    __syncthreads();                                   // every count read before it is replaced
     if (tid < n_ptiles) ptile_cnt[tid] = off;          // from here: first entry of the pair tile
   }
   __syncthreads();

@@ -217,7 +217,8 @@ struct mlora_meta {
   int vfull_ld = 0;
   int32_t *tile_unit_off = nullptr, *unit_blk = nullptr, *unit_tile = nullptr, *grp_mp = nullptr,
           *grp_ent = nullptr, *grp_cnt = nullptr, *ptile_off = nullptr, *pent_blk = nullptr, *pent_u0 = nullptr, *pent_u1 = nullptr,
-          *pair_fused = nullptr, *todo_blk = nullptr;
+          *pair_fused = nullptr, *todo_blk = nullptr, *ptile_order = nullptr;
+  uint32_t* sync = nullptr;
   uint16_t* vtile = nullptr;
   int unit_cap = 0;
   int T = 0, J = 1, S = -1;
@@ -255,6 +256,8 @@ struct mlora_meta {
     v.pent_u1 = pent_u1;
     v.pair_fused = pair_fused;
     v.todo_blk = todo_blk;
+    v.ptile_order = ptile_order;
+    v.sync = sync;
     v.vtile = vtile;
     v.unit_cap = unit_cap;
     v.n = T * J;
@@ -704,6 +707,8 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->pent_blk), U * 4);
   alloc(reinterpret_cast<void**>(&m->pent_u0), U * 4);
   alloc(reinterpret_cast<void**>(&m->pent_u1), U * 4);
+  alloc(reinterpret_cast<void**>(&m->ptile_order), ((n_tiles + 1) / 2 + 1) * 4);
+  alloc(reinterpret_cast<void**>(&m->sync), ((n_tiles + 1) / 2 + 2) * 4);
   alloc(reinterpret_cast<void**>(&m->pair_fused), n * 4);
   alloc(reinterpret_cast<void**>(&m->todo_blk), n * 4);
   alloc(reinterpret_cast<void**>(&m->vtile), U * 128 * kBlockCols * 2);
@@ -713,6 +718,7 @@ mlora_status mlora_meta_create(int max_tokens, int J_max, int r_max, mlora_meta_
   alloc(reinterpret_cast<void**>(&m->vfull), static_cast<size_t>(vt) * m->vfull_ld * 4);
   if (e == cudaSuccess) e = cudaMemset(m->err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(m->counts, 0, 32);
+  if (e == cudaSuccess) e = cudaMemset(m->sync, 0, ((n_tiles + 1) / 2 + 2) * 4);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->done, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -755,6 +761,8 @@ mlora_status mlora_meta_destroy(mlora_meta_t m) {
   cudaFree(m->pent_blk);
   cudaFree(m->pent_u0);
   cudaFree(m->pent_u1);
+  cudaFree(m->ptile_order);
+  cudaFree(m->sync);
   cudaFree(m->pair_fused);
   cudaFree(m->todo_blk);
   cudaFree(m->vtile);
@@ -932,7 +940,9 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
     // tensor-core side path: the shrink of every unit (M-tile, column block), then the base GEMM
     // with the expand as extra K blocks; the CUDA-core kernels take the pairs of M-tiles that
     // overflow the unit lists, and are launched only when the sizes allow an overflow
-    if ((e = launch_lora_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
+    // (the CTA-pair GEMM computes the shrink itself, as tiles of its own schedule, for K <= 8192)
+    const bool fused_shrink = base_gemm_uses_pair(m->T) && pair_gemm_fuses_shrink(p->K);
+    if (!fused_shrink && (e = launch_lora_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "tensor-core shrink launch");
     if ((e = launch_base_gemm_lora(x, W, y, m->T, p->K, p->D, ds->err, ds->num_sms, &pv, &mv, s)) != cudaSuccess)
       return cuda_fail(e, "base GEMM launch");

@@ -92,6 +92,62 @@ __device__ __forceinline__ bool mbar_wait_short(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// As mbar_try_wait_hint with acquire semantics at cluster scope: for a barrier that another CTA
+// of the cluster arrives on (release.cluster) after writing data this thread then reads.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Arrive with release at cluster scope on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Relaxed load of a global counter (gpu scope): for polling; order what follows a successful
+// poll with fence_acq_rel_gpu.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Orders this thread's earlier generic-proxy accesses of global memory before its later
+// async-proxy ones (a TMA load of data another SM wrote with ordinary stores).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits (bounded, 2 s) until *counter >= target; false and the timeout bit set in *err otherwise.
+// Polls with relaxed loads (acquire polling slows the SM's other memory traffic) and ends with
+// an acquire fence.
+__device__ __forceinline__ bool wait_counter(const uint32_t* counter, uint32_t target, uint32_t* err) {
+  if (ld_relaxed_gpu(counter) >= target) {
+    fence_acq_rel_gpu();
+    return true;
+  }
+  const uint64_t t0 = globaltimer();
+  for (uint32_t spin = 0;; ++spin) {
+    __nanosleep(64);
+    if (ld_relaxed_gpu(counter) >= target) {
+      fence_acq_rel_gpu();
+      return true;
+    }
+    if ((spin & 255u) == 255u && globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
 // Waits for the phase of the given parity to complete. Returns false (and sets the
 // timeout bit in *err) if it does not complete within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
