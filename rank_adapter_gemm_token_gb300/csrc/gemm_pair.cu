@@ -37,6 +37,7 @@
 // Both CTAs always reach the final cluster barrier, so a timeout never turns into a hang.
 #include <cuda.h>
 
+#include <algorithm>
 #include <climits>
 
 #include "internal.h"
@@ -623,6 +624,15 @@ double pair_time(int T, int D, int bn, int max_pairs) {
   return static_cast<double>(waves) * (0.83 + 0.17 * bn / 256.0);
 }
 
+// The same with the dynamic schedule of the fused side path: the pairs that finish early take the
+// remaining tiles, so a partial last wave costs its fraction (at least one tile per pair).
+double pair_time_dynamic(int T, int D, int bn, int max_pairs) {
+  const long mp = ((T + kHalf - 1) / kHalf + 1) / 2;
+  const long tiles = mp * ((D + bn - 1) / bn);
+  const double waves = std::max(1.0, static_cast<double>(tiles) / max_pairs);
+  return waves * (0.83 + 0.17 * bn / 256.0);
+}
+
 }  // namespace
 
 int pair_gemm_max_pairs() {
@@ -658,13 +668,15 @@ int pair_gemm_max_pairs() {
   return clusters;
 }
 
-int pair_gemm_pick_n(int T, int D, int max_pairs) {
+int pair_gemm_pick_n(int T, int D, int max_pairs, bool dynamic) {
   static const int kChoices[] = {256, 224, 192, 128};
   int best = 256;
   double best_time = 0.0;
-  for (int bn : kChoices) {                    // the widest of equally fast choices
-    const double t = pair_time(T, D, bn, max_pairs);
-    if (bn == 256 || t < best_time - 1e-9) {
+  for (int bn : kChoices) {
+    // static schedule: the widest of equally fast choices; dynamic schedule: the narrowest (its
+    // smaller tiles balance better around the tiles with many extra K blocks)
+    const double t = dynamic ? pair_time_dynamic(T, D, bn, max_pairs) : pair_time(T, D, bn, max_pairs);
+    if (bn == 256 || t < best_time - 1e-9 || (dynamic && t <= best_time + 1e-9)) {
       best_time = t;
       best = bn;
     }
@@ -679,7 +691,7 @@ cudaError_t launch_pair_gemm(const uint16_t* x, const uint16_t* W, float* y, int
   const bool fuse = pool && meta && pair_gemm_fuses_shrink(K);
   const int max_pairs = pair_gemm_max_pairs();
   if (max_pairs < 1) return cudaErrorNotSupported;
-  if (bn == 0) bn = pair_gemm_pick_n(T, D, max_pairs);
+  if (bn == 0) bn = pair_gemm_pick_n(T, D, max_pairs, fuse);
   switch (bn) {
     case 256: return launch_pair_bn<256, 6>(x, W, y, T, K, D, err, pool, meta, max_pairs, fuse, s);
     case 224: return launch_pair_bn<224, 6>(x, W, y, T, K, D, err, pool, meta, max_pairs, fuse, s);

@@ -159,7 +159,7 @@ int pair_gemm_max_pairs();
 // schedule) for inputs of width K.
 bool base_gemm_uses_pair(int T);
 bool pair_gemm_fuses_shrink(int K);
-int pair_gemm_pick_n(int T, int D, int max_pairs);
+int pair_gemm_pick_n(int T, int D, int max_pairs, bool dynamic);
 cudaError_t launch_pair_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                              const PoolView* pool, const MetaView* meta, int bn, cudaStream_t s);
 int gemm_tile_n();
