@@ -398,6 +398,7 @@ KERNEL_SOURCES = {
     ("prefill", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
     ("prefill", "shrink"): ("shrink_tc.cu", "ptx.cuh", "internal.h"),
     ("logits", "base_gemm"): ("gemm_pair.cu", "ptx.cuh", "internal.h"),
+    ("embedding", "embedding"): ("embedding.cu", "ptx.cuh", "internal.h"),
 }
 
 
