@@ -115,8 +115,12 @@ bool make_tmap_f32_sw128(CUtensorMap* map, const void* base, long rows, int cols
 // Launchers. Each returns the cudaError_t of its launch.
 // The step's metadata: sorted pairs, segments, pair-blocks, active slots and, for the tensor-core
 // side path, the units of each M-tile over the pool's column blocks.
+// mode kMetaSortOnly: the sort, segments, pair-blocks and active slots (every path needs them);
+// kMetaUnitsOnly: the tensor-core side path's units, pair-tile entries and groups of the step
+// whose sort ran earlier (token_slots and scales are not read); kMetaAll: both.
+constexpr int kMetaAll = 0, kMetaSortOnly = 1, kMetaUnitsOnly = 2;
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, const PoolView& pool,
-                              const MetaView& m, cudaStream_t s);
+                              const MetaView& m, cudaStream_t s, int mode = kMetaAll);
 
 // y[T, D] (fp32) = x[T, K] (bf16, row-major) * W[D, K]^T (bf16, row-major), tcgen05 path.
 cudaError_t launch_base_gemm(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D,

@@ -109,7 +109,7 @@ __device__ __forceinline__ void emit_bits(const uint32_t* bm, int n_words, F&& p
 
 __global__ void __launch_bounds__(kMetaThreads, 1)
 build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restrict__ scales, int n, PoolView pool,
-                  MetaView m, int cache, int keep) {
+                  MetaView m, int cache, int keep, int mode) {
   extern __shared__ int smem[];
   const int S = pool.S;
   const int nb = S + 1;
@@ -146,8 +146,9 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   ptx::grid_dependents_launch();             // the first linear's kernels may start their set-up
   // the first chunk's inputs are loaded while the slot table is staged
-  const int s_first = tid < n ? token_slots[tid] : -1;
-  const float c_first = tid < n && scales ? scales[tid] : 1.0f;
+  const bool sort = mode != kMetaUnitsOnly, units = mode != kMetaSortOnly;
+  const int s_first = sort && tid < n ? token_slots[tid] : -1;
+  const float c_first = sort && tid < n && scales ? scales[tid] : 1.0f;
   // 0. which slots hold an adapter (staged once, so pair validation needs no dependent load);
   //    `cursor` is free until step 2
   for (int b = tid; b < nb; b += kMetaThreads) {
@@ -162,6 +163,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
   if (tid == 0) first_bad = INT_MAX;
   __syncthreads();
 
+  if (sort) {
   // 1. validate, histogram, per-pair slot and scale; the first chunk's bins stay in registers
   int first_bin = nb;
   for (int p = tid; p < n; p += kMetaThreads) {
@@ -260,7 +262,12 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     for (int b = tid; b < nb; b += kMetaThreads) cursor[b] += chunk_tot[b];
     __syncthreads();
   }
+  } else {
+    if (tid == 0) n_blk_sh = m.counts[2];           // the sort of this step ran in an earlier launch
+    __syncthreads();
+  }
 
+  if (units) {
   // 4. units of the tensor-core side path: for each 128-token M-tile the column blocks its active
   //    pairs' slots own (warp per tile, bitmap over the blocks), counted, capped, numbered.
   const int n_tiles = (m.T + 127) / 128;
@@ -413,8 +420,9 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
     for (int b = c0; b < c1; ++b)
       if (todo(b)) m.todo_blk[pos++] = b;
   }
+  }
 
-  if (tid == 0) {
+  if (sort && tid == 0) {
     m.counts[3] = first_bad;
     if (first_bad != INT_MAX) atomicOr(m.err, ptx::kErrBadSlot);
   }
@@ -423,7 +431,7 @@ build_meta_kernel(const int32_t* __restrict__ token_slots, const float* __restri
 }  // namespace
 
 cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, int T, int J, const PoolView& pool,
-                              const MetaView& m, cudaStream_t s) {
+                              const MetaView& m, cudaStream_t s, int mode) {
   const int nb = pool.S + 1;
   const int n = T * J;
   const size_t bins = static_cast<size_t>(nb) * (4 * sizeof(int) + 32 * sizeof(uint16_t));
@@ -437,7 +445,8 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
   const size_t bitmaps = keep ? kept : scratch;
   const size_t front = ((bins > bitmaps ? bins : bitmaps) + 15) / 16 * 16 + slots_bytes;
   if (front > kMetaMaxDynSmem) return cudaErrorInvalidValue;
-  const int cache = front + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
+  // the units-only pass reads the sort's arrays from global memory
+  const int cache = mode != kMetaUnitsOnly && front + static_cast<size_t>(n) * 4 * sizeof(int) <= kMetaMaxDynSmem ? 1 : 0;
   const size_t smem = front + (cache ? static_cast<size_t>(n) * 4 * sizeof(int) : 0);
   static int configured_device = -1;
   int dev = 0;
@@ -449,7 +458,7 @@ cudaError_t launch_build_meta(const int32_t* token_slots, const float* scales, i
     configured_device = dev;
   }
   note_launch_begin(kKindMeta, s);
-  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, pool, m, cache, keep);
+  build_meta_kernel<<<1, kMetaThreads, smem, s>>>(token_slots, scales, n, pool, m, cache, keep, mode);
   cudaError_t e = cudaGetLastError();
   note_launch_end(kKindMeta, s);
   return e;

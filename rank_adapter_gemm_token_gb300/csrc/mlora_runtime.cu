@@ -224,6 +224,7 @@ struct mlora_meta {
   int T = 0, J = 1, S = -1;
   std::vector<int> class_slots, class_rank;    // layout of the pool the last build used
   bool built = false;
+  bool units_built = false;                    // the tensor-core path's units of the last build
   cudaEvent_t done = nullptr;
   cudaStream_t last_stream = nullptr;          // the stream of the last call that used the metadata
 
@@ -788,10 +789,13 @@ mlora_status mlora_build_meta(mlora_meta_t m, const int32_t* token_slots, const 
   m->class_slots = pool->class_slots;
   m->class_rank = pool->class_rank;
   MetaView v = m->view();
-  cudaError_t e = launch_build_meta(token_slots, scales, T, J, pool->view(), v, s);
+  // the sort only: the tensor-core side path's unit lists are built by the first linear that
+  // takes that path (small-batch steps never need them)
+  cudaError_t e = launch_build_meta(token_slots, scales, T, J, pool->view(), v, s, kMetaSortOnly);
   if (e != cudaSuccess) return cuda_fail(e, "build_meta launch");
   m->last_stream = s;
   m->built = true;
+  m->units_built = false;
   return MLORA_OK;
 }
 
@@ -940,6 +944,11 @@ mlora_status mlora_linear(mlora_pool_t p, mlora_meta_t m, const mlora_bf16* x, c
     // tensor-core side path: the shrink of every unit (M-tile, column block), then the base GEMM
     // with the expand as extra K blocks; the CUDA-core kernels take the pairs of M-tiles that
     // overflow the unit lists, and are launched only when the sizes allow an overflow
+    if (!m->units_built) {
+      if ((e = launch_build_meta(nullptr, nullptr, m->T, m->J, pv, mv, s, kMetaUnitsOnly)) != cudaSuccess)
+        return cuda_fail(e, "unit lists launch");
+      m->units_built = true;
+    }
     // (the CTA-pair GEMM computes the shrink itself, as tiles of its own schedule, for K <= 8192)
     const bool fused_shrink = base_gemm_uses_pair(m->T) && pair_gemm_fuses_shrink(p->K);
     if (!fused_shrink && (e = launch_lora_shrink_tc(x, pv, mv, ds->err, ds->num_sms, s)) != cudaSuccess)

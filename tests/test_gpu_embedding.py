@@ -66,6 +66,7 @@ def _check(wl, y, what):
     (1, 50, 2, 1, [(1, 8)], True),                                # one token, two columns
     (2048, 3001, 520, 1, [(40, 16)], True),                       # many pair-blocks and sentinel groups
     (96, 700, 4096, 8, [(3, 8), (9, 64)], True),                  # eight slots per token, full width
+    (200, 777, 264, 1, [(3, 128), (2, 8)], True),                 # one slot per token, slots wider than 64
 ])
 def test_embedding_matches_the_oracle(cuda_device, T, vocab, dim, J, classes, scales):
     wl = synth.embedding_case(T, vocab, dim, J, classes, with_scales=scales)
