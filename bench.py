@@ -135,13 +135,20 @@ def sub_workload(wl, r0: int, r1: int):
     return sub
 
 
+FUSE_MAX_K = 8192     # the library's CTA-pair GEMM computes the shrink itself up to this K
+
+
 def layer_path(wl, lin, num_sms: int = 152) -> str:
     """Which kernels the library runs for this linear: 'small' (T <= 256, one rank width, output
-    column blocks within one wave: split-K GEMM with the shrink folded in, then a separate expand)
-    or 'tc' (shrink on the tensor cores, expand inside the base GEMM as extra K blocks)."""
+    column blocks within one wave: split-K GEMM with the shrink folded in, then a separate expand),
+    'fused' (two or more 128-token tiles and K <= 8192: the CTA-pair GEMM computes the shrink as
+    sub-tiles of its schedule and the expand as extra K blocks) or 'tc' (the separate tensor-core
+    shrink, then the expand inside the base GEMM as extra K blocks)."""
     classes = getattr(wl, "classes", None)
     if wl.T <= 256 and not classes and (lin.D + 127) // 128 <= num_sms:
         return "small"
+    if wl.T > 128 and lin.K <= FUSE_MAX_K:
+        return "fused"
     return "tc"
 
 
@@ -158,7 +165,8 @@ def algorithmic(wl, num_sms: int = 152) -> dict:
     pair for the expand.
     Attribution: 'small': base_gemm = W + x + y + A rows + v write, expand = B rows + y
     read-modify-write + v read. 'tc': shrink = A rows + x rows of the tokens with an active slot
-    + v write, base_gemm = W + x + y + B rows + v read."""
+    + v write, base_gemm = W + x + y + B rows + v read. 'fused': all of it to base_gemm (W + x + y
+    + A rows + B rows + v written and read), with the shrink's flops."""
     slots = wl.token_slots
     active = slots >= 0
     rows = int(np.any(active, axis=1).sum())
@@ -174,11 +182,15 @@ def algorithmic(wl, num_sms: int = 152) -> dict:
         base = l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4
         a_rows, b_rows = sum_r * l.K * 2, sum_r * l.D * 2
         f_base, f_shrink, f_expand = 2 * wl.T * l.K * l.D, 2 * pair_r * l.K, 2 * pair_r * l.D
-        if layer_path(wl, l, num_sms) == "small":
+        path = layer_path(wl, l, num_sms)
+        if path == "small":
             out["base_gemm"] += base + a_rows + v
             out["expand"] += b_rows + rows * l.D * 8 + v
             flops["base_gemm"] += f_base + f_shrink
             flops["expand"] += f_expand
+        elif path == "fused":
+            out["base_gemm"] += base + a_rows + b_rows + 2 * v
+            flops["base_gemm"] += f_base + f_shrink + f_expand
         else:
             out["shrink"] += a_rows + rows * l.K * 2 + v
             out["base_gemm"] += base + b_rows + v

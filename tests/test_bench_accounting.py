@@ -52,15 +52,32 @@ def test_wide_output_takes_the_tensor_core_path():
 
 
 def test_large_batch_counts_each_adapter_once():
+    # K <= 8192 and two or more 128-token tiles: the pair GEMM computes the shrink itself, so every
+    # byte and flop of the side path is the GEMM's
     wl = synth.prefill(n_requests=3, seg_len=192, hidden=128, mlp=256)
     got = bench.algorithmic(wl, num_sms=152)
-    shrink = base = 0
+    base = fl = 0
     for l in wl.linears:
+        assert bench.layer_path(wl, l, 152) == "fused"
         sr = sum(l.adapters[s].rank for s in range(3))
         pr = _pair_ranks(wl, l)
-        shrink += sr * l.K * 2 + wl.T * l.K * 2 + pr * 4
-        base += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4 + sr * l.D * 2 + pr * 4
-    assert (got["shrink"], got["base_gemm"], got["expand"]) == (shrink, base, 0)
+        base += l.D * l.K * 2 + wl.T * l.K * 2 + wl.T * l.D * 4 + sr * l.K * 2 + sr * l.D * 2 + 2 * pr * 4
+        fl += 2 * wl.T * l.K * l.D + 2 * pr * l.K + 2 * pr * l.D
+    assert (got["shrink"], got["base_gemm"], got["expand"]) == (0, base, 0)
+    assert got["flops"]["base_gemm"] == fl
+
+
+def test_long_k_keeps_the_separate_shrink():
+    wl = synth.prefill(n_requests=3, seg_len=192, hidden=128, mlp=9000)   # the down projection: K > 8192
+    got = bench.algorithmic(wl, num_sms=152)
+    shrink = 0
+    for l in wl.linears:
+        if l.K <= bench.FUSE_MAX_K:
+            continue
+        assert bench.layer_path(wl, l, 152) == "tc"
+        sr = sum(l.adapters[s].rank for s in range(3))
+        shrink += sr * l.K * 2 + wl.T * l.K * 2 + _pair_ranks(wl, l) * 4
+    assert got["shrink"] == shrink > 0
 
 
 def test_roofline_picks_the_slower_bound():
