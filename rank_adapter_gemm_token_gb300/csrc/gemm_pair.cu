@@ -188,8 +188,6 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
   const int num_mp = (num_m + 1) / 2;                    // pair tiles along M
   const int num_n = (D + BN - 1) / BN;
   const int num_kb = (K + kPK - 1) / kPK;
-  const int S = sp.fused ? *sp.n_groups * (kGroupUnits / kPer) : 0;
-  const int total = S + num_mp * num_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -217,6 +215,12 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_c
   ptx::cluster_sync_all();                    // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // programmatic dependent launch: the set-up above overlapped the previous kernel's tail; from
+  // here on its results (x, the metadata) are read. The next kernel may start its own set-up.
+  ptx::grid_dependency_wait();
+  ptx::grid_dependents_launch();
+  const int S = sp.fused ? *sp.n_groups * (kGroupUnits / kPer) : 0;
+  const int total = S + num_mp * num_n;
 
   // Reads tile id number i of this pair (one thread of each reading role): waits for it, then
   // tells rank 0's scheduler that this reader is done with the slot. -1: no more tiles (or a
@@ -598,13 +602,15 @@ cudaError_t launch_pair_bn(const uint16_t* x, const uint16_t* W, float* y, int T
   cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   note_launch_begin(kKindGemm, s);
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_pair_kernel<BN, STAGES>, mx, mw, mv, mb, ma, my, sp, y, y_tma, T,
                                      D, K, err);

@@ -107,6 +107,8 @@ lora_shrink_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid
   ptx::cluster_sync_all();                                // barriers of the cluster initialised
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  ptx::grid_dependency_wait();                            // the previous kernel's results (x, metadata)
+  ptx::grid_dependents_launch();                          // the next kernel may start its set-up
   const int n_groups = m.counts[7];
 
   int stage = 0;                                          // ring position (producer and MMA thread)
@@ -296,11 +298,13 @@ cudaError_t launch_lora_shrink_tc(const uint16_t* x, const PoolView& pool, const
   if (pairs > kMaxPairs) pairs = kMaxPairs;
   if (pairs < 1) pairs = 1;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * pairs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.attrs = attr;
@@ -326,6 +330,7 @@ cudaError_t launch_lora_shrink_tc(const uint16_t* x, const PoolView& pool, const
     return cudaErrorInvalidValue;
   cfg.gridDim = dim3(max_clusters[pairs] * 2 * pairs, 1, 1);
   cfg.stream = s;
+  cfg.numAttrs = 2;                                       // with programmatic dependent launch
   note_launch_begin(kKindShrink, s);
   cudaError_t e = cudaLaunchKernelEx(&cfg, lora_shrink_pair_kernel, mx, ma, pool, m, pairs, err);
   note_launch_end(kKindShrink, s);
