@@ -215,12 +215,13 @@ gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_con
 
 // ---------------------------------------------------------------------------------------------
 // Skinny variant for small batches (T <= 256, the decode case): the roles swap so that W is the
-// A operand (128 output features per CTA, M = 128) and all tokens form N (NT = T rounded up to
-// 16), which reads every W element exactly once. K is split across the CTAs of a thread-block
-// cluster (cluster rank = K split); each CTA stages its fp32 partial tile P[t][o] in its own
-// shared memory, and after a cluster barrier CTA r sums the partials of all CTAs for its share
-// of the tokens through distributed shared memory, always in rank order 0, 1, ... (so the
-// result is deterministic), and writes the output with coalesced 16-byte stores.
+// A operand (128 output features per CTA) and all tokens form N (NT = T rounded up to 16), which
+// reads every W element exactly once. K is split across the CTAs of a thread-block cluster; each
+// CTA stages its fp32 partial tile P[t][o] in its own shared memory, and after a cluster barrier
+// each CTA sums, for its share of the tokens, the partials of the CTAs that hold the same output
+// block through distributed shared memory, always in K-split order (so the result is
+// deterministic), and writes the output with coalesced 16-byte stores. The kernel runs on CTA
+// pairs (gemm_bf16_skinny_pair_kernel below).
 //
 // The shrink of the LoRA side path rides along ("Multi-LoRA Serving Explained", batched
 // serving: one large product shared by the batch plus each token's low-rank side path). The
@@ -249,15 +250,8 @@ struct SkinnyAMaps {
   CUtensorMap box[kABoxMaps];
 };
 
-constexpr int kSkinnyStages = 4;
 constexpr int kPullLoads = 12;            // distributed-shared-memory loads in flight per thread
 constexpr int kSkinnyABytes = BM * BK * 2;
-constexpr int kSkinnyMaxSplit = 8;
-
-__host__ __device__ constexpr int skinny_stage_bytes(int NT) { return kSkinnyABytes + NT * BK * 2; }
-__host__ __device__ constexpr int skinny_smem_bytes(int NT) {
-  return kSkinnyStages * skinny_stage_bytes(NT) + 256 + 1024;
-}
 
 // Split-K reduction of the skinny kernel: every CTA of the cluster holds its fp32 partial tile
 // part[t][o] (t < NT, o < 128) in shared memory; this CTA sums, for tokens [t0, t1) and the first
@@ -266,7 +260,7 @@ __host__ __device__ constexpr int skinny_smem_bytes(int NT) {
 // of one token; each thread keeps the loads of several items in flight before summing.
 template <int SPLIT>
 __device__ __forceinline__ void skinny_pull(cooperative_groups::cluster_group& cluster, float* part, int t0, int t1,
-                                            int rows, float* out, long ld, int cols) {
+                                            int rows, float* out, long ld, int cols, int rank0 = 0, int rstride = 1) {
   constexpr int kItems = kPullLoads / SPLIT > 1 ? kPullLoads / SPLIT : 1;
   const int n_items = (t1 - t0) * (BM / 4);
   const bool vec = (cols & 3) == 0 && (ld & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
@@ -279,7 +273,7 @@ __device__ __forceinline__ void skinny_pull(cooperative_groups::cluster_group& c
       if (w < n_items && o4 < rows) {
 #pragma unroll
         for (int r = 0; r < SPLIT; ++r)
-          pv[h][r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, r));
+          pv[h][r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part + t * BM + o4, rank0 + rstride * r));
       }
     }
 #pragma unroll
@@ -308,89 +302,118 @@ __device__ __forceinline__ void skinny_pull(cooperative_groups::cluster_group& c
   }
 }
 
+// CTA-pair form of the skinny kernel. Two CTAs of a cluster form a pair (cta_group::2) for two
+// consecutive 128-row output blocks: rank 2 k + h holds block 2 p + h's A rows and tokens
+// h NT/2 .. h NT/2 + NT/2 - 1 of x for K share k, and the even CTA issues M = 256 x N = NT MMAs
+// that read both CTAs' operands, accumulating each block in its own CTA's TMEM. Per 64-wide K
+// block an SM then stages 16 KB of A rows and 16 KB of x instead of 16 + 32 KB, so six stages fit
+// where four did, and x is read from L2 half as often. The K shares of a block (ranks h, h + 2,
+// ...) reduce their partials as in the one-CTA form. A pair whose even block has no rows (an A
+// block past the active slots, or a block past the grid) skips the main loop; an odd block
+// without rows still stages its half of x and lets the pair compute rows that are then dropped.
+constexpr int kSkinnyPairStages = 6;
+constexpr int kSkinnyPairMaxSplit = 4;      // clusters of at most 8 CTAs
+
+__host__ __device__ constexpr int skinny_pair_stage_bytes(int NT) { return kSkinnyABytes + (NT / 2) * BK * 2; }
+__host__ __device__ constexpr int skinny_pair_smem_bytes(int NT) {
+  return kSkinnyPairStages * skinny_pair_stage_bytes(NT) + 256 + 1024;
+}
+
+// Rows of A-operand data block `oblk` holds in the skinny kernel (0: none), and for an A block
+// the number of active slots it covers.
+__device__ __forceinline__ int skinny_block_rows(int oblk, int n_oblk, int n_wblk, const SkinnyShrink& sh, int n_act,
+                                                 int* n_box) {
+  *n_box = 0;
+  if (oblk >= n_oblk) return 0;                         // a block past the grid (odd count)
+  if (oblk < n_wblk) return BM;
+  const int spb = BM / sh.R;
+  const int a0 = (oblk - n_wblk) * spb;
+  *n_box = max(0, min(spb, n_act - a0));
+  return *n_box * sh.R;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
-gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                        const __grid_constant__ SkinnyAMaps amaps, float* __restrict__ y, int T, int D, int K,
-                        int NT, int splitk, uint32_t tmem_cols, uint32_t* __restrict__ err, SkinnyShrink sh) {
+gemm_bf16_skinny_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_xh,
+                             const __grid_constant__ SkinnyAMaps amaps, float* __restrict__ y, int T, int D, int K,
+                             int NT, int splitk, int n_oblk, uint32_t tmem_cols, uint32_t* __restrict__ err,
+                             SkinnyShrink sh) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_bytes = skinny_stage_bytes(NT);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkinnyStages * stage_bytes);
-  uint64_t* empty = full + kSkinnyStages;
-  uint64_t* acc_full = empty + kSkinnyStages;
+  const int stage_bytes = skinny_pair_stage_bytes(NT);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkinnyPairStages * stage_bytes);   // used in the even CTA
+  uint64_t* empty = full + kSkinnyPairStages;                                              // in each CTA
+  uint64_t* acc_full = empty + kSkinnyPairStages;                                          // in each CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   float* part = reinterpret_cast<float*>(smem);          // [NT][128] after the main loop
 
   cg::cluster_group cluster = cg::this_cluster();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int half = rank & 1, ks = rank >> 1;
   const int n_wblk = (D + BM - 1) / BM;
-  const int oblk = blockIdx.x / splitk;
-  const int ks = static_cast<int>(cluster.block_rank());
-  const bool a_blk = oblk >= n_wblk;                    // a block of active-slot A rows
-  const int spb = a_blk ? BM / sh.R : 0;                // slots per A block
-  const int a0 = a_blk ? (oblk - n_wblk) * spb : 0;     // first active slot of the block
+  const int pair_o = blockIdx.x / (2 * splitk);
+  const int oblk = 2 * pair_o + half;
+  const bool a_blk = oblk < n_oblk && oblk >= n_wblk;   // a block of active-slot A rows
+  const int spb = a_blk ? BM / sh.R : 0;
+  const int a0 = a_blk ? (oblk - n_wblk) * spb : 0;
   const int o0 = oblk * BM;
   const int num_kb = (K + BK - 1) / BK;
   const int kb0 = ks * num_kb / splitk, kb1 = (ks + 1) * num_kb / splitk;
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << (rank & ~1));
 
-  // Set-up that depends on no earlier kernel (programmatic dependent launch lets it overlap the
-  // previous kernel's tail): barriers, TMEM, descriptor prefetch, and this CTA's W range
-  // prefetched into L2 (a hint only; the operand loads below come after the dependency wait).
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSkinnyStages; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+    for (int s = 0; s < kSkinnyPairStages; ++s) {
+      ptx::mbar_init(&full[s], 1);                      // the even CTA posts both halves' bytes
+      ptx::mbar_init(&empty[s], 1);                     // one multicast commit per use
     }
     ptx::mbar_init(acc_full, 1);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
     ptx::tma_prefetch_desc(a_blk ? &amaps.box[0] : &tmap_w);
-    ptx::tma_prefetch_desc(&tmap_x);
+    ptx::tma_prefetch_desc(&tmap_xh);
   }
-  if (warp == 2 && !a_blk)
+  if (warp == 2 && oblk < n_wblk)
     for (int kb = kb0 + lane; kb < kb1; kb += 32) ptx::tma_prefetch_l2_2d(&tmap_w, kb * BK, o0);
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, tmem_cols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(tmem_slot, tmem_cols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync_all();                              // barriers of the cluster initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   ptx::grid_dependency_wait();                          // earlier kernels' writes are visible
   ptx::grid_dependents_launch();                        // the next kernel may start its set-up
-  int n_act = 0;
-  bool idle = false;                                    // an A block with no active slot
-  if (a_blk) {
-    n_act = *sh.n_act;
-    idle = a0 >= n_act;                                 // uniform across the cluster
-    if (!idle && warp == 2) {                           // this block's adapter rows into L2
-      const int n_box = min(spb, n_act - a0);
-      for (int e = lane; e < n_box * (kb1 - kb0); e += 32) {
-        const int i = e % n_box, kb = kb0 + e / n_box;
-        ptx::tma_prefetch_l2_2d(&amaps.box[0], kb * BK, sh.act_slot[a0 + i] * sh.R);
-      }
+  const int n_act = sh.n_ablk > 0 ? *sh.n_act : 0;
+  int my_box = 0, peer_box = 0;
+  const int my_rows = skinny_block_rows(oblk, n_oblk, n_wblk, sh, n_act, &my_box);
+  const int peer_rows = skinny_block_rows(oblk ^ 1, n_oblk, n_wblk, sh, n_act, &peer_box);
+  const int even_rows = half ? peer_rows : my_rows;
+  const bool idle = even_rows == 0;                     // uniform across the cluster (the pair's even block)
+  if (!idle && a_blk && my_box > 0 && warp == 2) {      // this block's adapter rows into L2
+    for (int e = lane; e < my_box * (kb1 - kb0); e += 32) {
+      const int i = e % my_box, kb = kb0 + e / my_box;
+      ptx::tma_prefetch_l2_2d(&amaps.box[0], kb * BK, sh.act_slot[a0 + i] * sh.R);
     }
   }
   const int n_exp_items = sh.n_dchunk ? (sh.meta.J == 1 ? sh.meta.counts[2] : sh.meta.T) * sh.n_dchunk : 0;
 
   if (idle) {
-    // nothing to multiply: only the expand phase below (if any)
+    // nothing to multiply
   } else if (warp == 0) {
     if (lane == 0) {
-      // A rows of the block: the active slots' R rows, one TMA box per run of 2^k slots with
-      // consecutive ids (largest power of two first), or one W box of 128 rows
+      // this CTA's A rows: the active slots' R rows, one TMA box per run of 2^k slots with
+      // consecutive ids (largest power of two first), or one W box of 128 rows; and its half of x
       int chunk_row[BM / 8], chunk_pos[BM / 8], chunk_k[BM / 8];
-      int n_box = 1, n_chunk = 0;
+      int n_chunk = 0;
       if (a_blk) {
-        n_box = min(spb, n_act - a0);
-        for (int i = 0; i < n_box;) {
+        for (int i = 0; i < my_box;) {
           const int s0 = sh.act_slot[a0 + i];
           int run = 1;
-          while (i + run < n_box && sh.act_slot[a0 + i + run] == s0 + run) ++run;
+          while (i + run < my_box && sh.act_slot[a0 + i + run] == s0 + run) ++run;
           const int k = 31 - __clz(run);                // 2^k <= run
           chunk_row[n_chunk] = s0 * sh.R;
           chunk_pos[n_chunk] = i;
@@ -399,53 +422,64 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
           i += 1 << k;
         }
       }
-      const uint32_t bytes = static_cast<uint32_t>(a_blk ? n_box * sh.R * BK * 2 + NT * BK * 2 : stage_bytes);
+      auto a_bytes = [&](int oblk_, int rows_, int box_) {
+        return oblk_ >= n_oblk ? 0 : (oblk_ < n_wblk ? kSkinnyABytes : box_ * sh.R * BK * 2);
+      };
+      const uint32_t bytes = static_cast<uint32_t>(a_bytes(oblk, my_rows, my_box) + a_bytes(oblk ^ 1, peer_rows, peer_box) +
+                                                   2 * (NT / 2) * BK * 2);
+      const uint32_t bar0 = ptx::mapa_shared(ptx::smem_u32(&full[0]), static_cast<uint32_t>(rank & ~1));
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, err)) break;
+        if (!ptx::mbar_wait_short(&empty[stage], phase ^ 1u, err)) break;
         uint8_t* sa = smem + stage * stage_bytes;
-        ptx::mbar_arrive_expect_tx(&full[stage], bytes);
+        const uint32_t bar = bar0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+        if (half == 0) ptx::mbar_arrive_expect_tx(&full[stage], bytes);
         if (a_blk) {
           for (int c = 0; c < n_chunk; ++c)
-            ptx::tma_load_2d(sa + chunk_pos[c] * sh.R * BK * 2, &amaps.box[chunk_k[c]], &full[stage], kb * BK,
-                             chunk_row[c]);
-        } else {
-          ptx::tma_load_2d(sa, &tmap_w, &full[stage], kb * BK, o0);
+            ptx::tma_load_2d_pair(sa + chunk_pos[c] * sh.R * BK * 2, &amaps.box[chunk_k[c]], bar, kb * BK,
+                                  chunk_row[c]);
+        } else if (oblk < n_oblk) {
+          ptx::tma_load_2d_pair(sa, &tmap_w, bar, kb * BK, o0);
         }
-        ptx::tma_load_2d(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, 0);
-        if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
+        ptx::tma_load_2d_pair(sa + kSkinnyABytes, &tmap_xh, bar, kb * BK, half * (NT / 2));
+        if (++stage == kSkinnyPairStages) { stage = 0; phase ^= 1u; }
+      }
+      // tail: every commit addressed to this CTA's stage barriers has landed before it may exit
+      for (int i = 0; i < kSkinnyPairStages; ++i) {
+        if (!ptx::mbar_wait_short(&empty[stage], phase ^ 1u, err)) break;
+        if (++stage == kSkinnyPairStages) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(BM, NT);
+    if (half == 0 && lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, NT);
       int stage = 0;
       uint32_t phase = 0;
       bool mma_ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!ptx::mbar_wait(&full[stage], phase, err)) { mma_ok = false; break; }
+        if (!ptx::mbar_wait_short(&full[stage], phase, err)) { mma_ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t a_addr = ptx::smem_u32(smem + stage * stage_bytes);
         const uint64_t a_desc = ptx::sw128_kmajor_desc(a_addr);
         const uint64_t b_desc = ptx::sw128_kmajor_desc(a_addr + kSkinnyABytes);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          ptx::umma_bf16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-        ptx::umma_commit(&empty[stage]);
-        if (++stage == kSkinnyStages) { stage = 0; phase ^= 1u; }
+          ptx::umma_bf16_pair(tmem_base, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        ptx::umma_commit_pair(&empty[stage], pair_mask);
+        if (++stage == kSkinnyPairStages) { stage = 0; phase ^= 1u; }
       }
-      if (mma_ok) ptx::umma_commit(acc_full);
+      if (mma_ok) ptx::umma_commit_pair(acc_full, pair_mask);
     }
   } else {
     // While the main loop runs, bring into L2 the B rows the expand kernel will read (a share
     // of its items per block).
     for (int item = blockIdx.x; item < n_exp_items; item += gridDim.x)
       expand_vfull_prefetch(sh.pool, sh.meta, item, sh.n_dchunk, threadIdx.x - 64, kGemmThreads - 64);
-    // TMEM lane = output row o (warp w reads lanes 32*(w%4)..), columns = tokens
+    // TMEM lane = output row o of this CTA's block (warp w reads lanes 32*(w%4)..), columns = tokens
     const int quarter = warp & 3;
     const int o = quarter * 32 + lane;
-    if (ptx::mbar_wait(acc_full, 0, err)) {
+    if (ptx::mbar_wait_short(acc_full, 0, err)) {
       ptx::tc_fence_after();
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
@@ -463,32 +497,28 @@ gemm_bf16_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid
       }
     }
   }
-  if (!idle) {
-    ptx::tc_fence_before();
-    ptx::cluster_sync_all();                            // every partial tile is in shared memory
-
-    // CTA ks owns tokens [t0, t1): float4 over rows, partials summed in rank order.
+  ptx::tc_fence_before();
+  ptx::cluster_sync_all();                              // every partial tile is in shared memory
+  if (!idle && my_rows > 0) {
+    // CTA (k, h) owns tokens [t0, t1) of block h: partials of ranks h, h + 2, ... summed in order
     const int per = (T + splitk - 1) / splitk;
     const int t0 = ks * per, t1 = min(T, t0 + per);
-    const int rows = a_blk ? min(spb, n_act - a0) * sh.R : BM;
+    const int rows = my_rows;
     float* out = a_blk ? sh.vfull + a0 * sh.R : y + o0;
     const long ld = a_blk ? sh.vfull_ld : D;
     const int cols = a_blk ? rows : min(BM, D - o0);
     switch (splitk) {
-      case 1: skinny_pull<1>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 2: skinny_pull<2>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 3: skinny_pull<3>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 4: skinny_pull<4>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 5: skinny_pull<5>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 6: skinny_pull<6>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      case 7: skinny_pull<7>(cluster, part, t0, t1, rows, out, ld, cols); break;
-      default: skinny_pull<8>(cluster, part, t0, t1, rows, out, ld, cols); break;
+      case 1: skinny_pull<1>(cluster, part, t0, t1, rows, out, ld, cols, half, 2); break;
+      case 2: skinny_pull<2>(cluster, part, t0, t1, rows, out, ld, cols, half, 2); break;
+      case 3: skinny_pull<3>(cluster, part, t0, t1, rows, out, ld, cols, half, 2); break;
+      default: skinny_pull<4>(cluster, part, t0, t1, rows, out, ld, cols, half, 2); break;
     }
-    ptx::cluster_sync_all();                          // no CTA leaves while others read its tile
   }
+  ptx::tc_fence_before();
+  ptx::cluster_sync_all();                              // no CTA leaves while others read its tile or TMEM
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, tmem_cols);
+    ptx::tmem_dealloc_pair(tmem_base, tmem_cols);
   }
 }
 
@@ -562,37 +592,33 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
   return e;
 }
 
-int skinny_splitk(int n_oblk, int K, int num_sms) {
-  const int num_kb = (K + BK - 1) / BK;
-  int splitk = num_sms / n_oblk;
-  if (splitk > kSkinnyMaxSplit) splitk = kSkinnyMaxSplit;
-  if (splitk > num_kb) splitk = num_kb;
-  if (splitk < 1) splitk = 1;
-  return splitk;
-}
 
-cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
-                          int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
+// The CTA-pair form: pairs of output blocks, K split over clusters of 2 x splitk CTAs.
+cudaError_t launch_skinny_pair(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                               int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
   const int NT = (T + 15) / 16 * 16;
   const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
-  const int splitk = skinny_splitk(n_oblk, K, num_sms);
+  const int n_pairs = (n_oblk + 1) / 2;
+  const int num_kb = (K + BK - 1) / BK;
+  int splitk = num_sms / (2 * n_pairs);
+  if (splitk > kSkinnyPairMaxSplit) splitk = kSkinnyPairMaxSplit;
+  if (splitk > num_kb) splitk = num_kb;
+  if (splitk < 1) splitk = 1;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(NT)) tmem_cols <<= 1;
-  const int smem = skinny_smem_bytes(NT);
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         skinny_smem_bytes(256));
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_skinny_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         skinny_pair_smem_bytes(256));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap mw, mx;
+  CUtensorMap mw, mxh;
   SkinnyAMaps ma;
-  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, NT, BK)) {
+  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mxh, x, T, K, NT / 2, BK))
     return cudaErrorInvalidValue;
-  }
   for (int k = 0; k < kABoxMaps; ++k) {
     if (sh.n_ablk > 0 && (sh.R << k) <= BM) {
       if (!make_tmap_bf16_impl(&ma.box[k], A_pool, static_cast<long>(S) * sh.R, K, sh.R << k, BK))
@@ -602,13 +628,13 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_oblk * splitk, 1, 1);
+  cfg.gridDim = dim3(n_pairs * 2 * splitk, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = skinny_pair_smem_bytes(NT);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = splitk;
+  attr[0].val.clusterDim.x = 2 * splitk;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -616,10 +642,15 @@ cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   note_launch_begin(kKindGemm, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_kernel, mw, mx, ma, y, T, D, K, NT, splitk, tmem_cols,
-                                     err, sh);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_pair_kernel, mw, mxh, ma, y, T, D, K, NT, splitk, n_oblk,
+                                     tmem_cols, err, sh);
   note_launch_end(kKindGemm, s);
   return e;
+}
+
+cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                          int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
+  return launch_skinny_pair(x, W, y, T, K, D, err, num_sms, A_pool, S, sh, s);
 }
 
 }  // namespace
