@@ -493,7 +493,8 @@ def time_adapter_loads(dw, n_slots: int = 16):
     return {"linear": f"{lin.name} {lin.K}->{lin.D}", "slots": len(staged), "bytes": nbytes,
             "ms_per_slot": 1000.0 * dt / max(1, len(staged)), "h2d_GBps": nbytes / dt / 1e9,
             "how": "mlora_load_adapter from pinned host memory on the pool's copy stream, wall clock until "
-                   "mlora_pool_sync returns (slot zeroing, A copy, strided B copy, slot factor)"}
+                   "mlora_pool_sync returns (slot A zeroing, A copy, B copy into a staging buffer, "
+                   "scatter kernel into the slot's B columns, slot factor)"}
 
 
 def run_ours(args):

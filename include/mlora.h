@@ -241,6 +241,15 @@ MLORA_API mlora_status mlora_lora_expand(mlora_pool_t pool, mlora_meta_t meta, f
  * captured graph that launches the GEMM may be re-captured. */
 MLORA_API mlora_status mlora_set_gemm_tile_n(int n);
 
+/* Form of the small-batch GEMM (batches of up to 256 tokens; process-wide; no counterpart on the
+ * pages: a tuning and test control). 0 (default) and 1: the split-K form (CTA pairs sharing the
+ * token operand, K split across a cluster, partial tiles summed in K order). 2: the token-split
+ * form whenever its grid fits one wave (each CTA multiplies a group of tokens by one 128-row
+ * block over all of K; clusters share W rows and x rows by TMA multicast; no partial tiles),
+ * else the split-K form. Other values: MLORA_ERR_INVALID_ARG, nothing changed. Both forms are
+ * deterministic; their results differ only by fp32 summation order. Set it between steps. */
+MLORA_API mlora_status mlora_set_skinny_form(int form);
+
 /* Path choice of mlora_linear (process-wide; no counterpart on the pages: a tuning and test
  * control): 0 automatic (default), 1 the small-batch path whenever the step allows it, 2 always
  * the tensor-core side path. Other values: MLORA_ERR_INVALID_ARG. Results differ between paths

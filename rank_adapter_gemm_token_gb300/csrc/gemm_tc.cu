@@ -522,6 +522,246 @@ gemm_bf16_skinny_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const _
   }
 }
 
+// Token-split form of the skinny kernel (mlora_set_skinny_form(2)): K is not split, so there are
+// no partial tiles to reduce. CTA (c, g) of a cluster of kTsC x G CTAs computes output block
+// kTsC * cluster + c for token group g over the whole of K (M = 128 rows, N = the group's tokens)
+// in its own TMEM and stores y (or v) from there. What CTAs share is fetched once per cluster by
+// TMA multicast, with as few and as large copies as possible (each TMA instruction has a fixed
+// cost): the block's 128 A-operand rows of K block kb (one W box, or the active slots' boxes) are
+// issued by CTA kb mod G of row c for the whole row, and group g's x rows by CTA kb mod kTsC of
+// column g for the whole column. A stage may be refilled only when every CTA that the refill
+// writes into has finished reading it, so each CTA's MMA commit arrives on the stage's empty
+// barrier in all CTAs of its row and its column (the CTAs whose loads write into it are exactly
+// those). A row without rows (an A block past the active slots, or a block past the grid) still
+// fetches its share of x and releases every stage.
+// Measured on the decode shape (256 tokens, 4096 -> 4096 plus 90 active rank-16 slots): 38 us
+// against 26 us for the split-K form. Multicast saves L2 reads but not SM ingress: an SM here
+// receives 28 KB per K block for 128 x 96 x 64 products, a CTA of the split-K pair 32 KB for
+// 128 x 256 x 64, and L2-to-SM bandwidth (about 100-115 GB/s per SM, measured in both) bounds both.
+constexpr int kTsC = 2;                    // output blocks per cluster (they share x)
+constexpr int kTsMaxG = 4;                 // token groups per cluster (they share the A rows)
+constexpr int kTsMaxStages = 8;
+constexpr int kTsSmemMax = 232448;         // opt-in shared memory per CTA (227 KB)
+// The shared-memory ring holds few K blocks of A rows per row of the cluster (a third or less of
+// a CTA's stage is its share of them), too few to keep enough HBM reads in flight; the producer
+// therefore also asks L2 for its A-row boxes this many K blocks ahead of the block it loads.
+constexpr int kTsPrefetchAhead = 24;
+
+// Tokens per group: groups of ts_group_max(NT, G) tokens (a multiple of 16), the last one shorter.
+__host__ __device__ constexpr int ts_group_max(int NT, int G) { return 16 * ((NT / 16 + G - 1) / G); }
+__host__ __device__ constexpr int ts_stage_bytes(int n_gmax) { return kSkinnyABytes + n_gmax * BK * 2; }
+__host__ __device__ constexpr int ts_stages(int n_gmax) {
+  return (kTsSmemMax - 1280) / ts_stage_bytes(n_gmax) < kTsMaxStages ? (kTsSmemMax - 1280) / ts_stage_bytes(n_gmax)
+                                                                     : kTsMaxStages;
+}
+__host__ __device__ constexpr int ts_smem_bytes(int n_gmax) {
+  return ts_stages(n_gmax) * ts_stage_bytes(n_gmax) + 256 + 1024;
+}
+
+// A TMA load to the CTAs of cta_mask (a plain load when the mask is this CTA alone).
+__device__ __forceinline__ void ts_load(void* dst, const void* tmap, uint64_t* bar, int32_t c0, int32_t c1,
+                                        uint16_t cta_mask, uint16_t self_bit) {
+  if (cta_mask == self_bit) ptx::tma_load_2d(dst, tmap, bar, c0, c1);
+  else ptx::tma_load_2d_mc(dst, tmap, bar, c0, c1, cta_mask);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_bf16_skinny_ts_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                           const __grid_constant__ SkinnyAMaps amaps, float* __restrict__ y, int T, int D, int K,
+                           int NT, int G, int n_oblk, int stages, uint32_t tmem_cols, uint32_t* __restrict__ err,
+                           SkinnyShrink sh) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_bytes = ts_stage_bytes(ts_group_max(NT, G));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + stages * stage_bytes);
+  uint64_t* empty = full + kTsMaxStages;
+  uint64_t* acc_full = empty + kTsMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  const int g = rank % G, c = rank / G;
+  const int cl = blockIdx.x / (kTsC * G);
+  const int oblk = cl * kTsC + c;
+  const int n_wblk = (D + BM - 1) / BM;
+  const bool a_blk = oblk < n_oblk && oblk >= n_wblk;
+  const int spb = a_blk ? BM / sh.R : 0;
+  const int a0 = a_blk ? (oblk - n_wblk) * spb : 0;
+  const int o0 = oblk * BM;
+  const int n_gmax = ts_group_max(NT, G);
+  const int t_g = g * n_gmax;
+  const int n_g = min(n_gmax, NT - t_g);
+  const int num_kb = (K + BK - 1) / BK;
+  const uint16_t self_bit = static_cast<uint16_t>(1u << rank);
+  const uint16_t row_mask = static_cast<uint16_t>(((1u << G) - 1u) << (c * G));
+  uint16_t col_mask = 0;
+  for (int cc = 0; cc < kTsC; ++cc) col_mask |= static_cast<uint16_t>(1u << (cc * G + g));
+  const uint16_t peer_mask = row_mask | col_mask;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(&full[s], 1);                      // this CTA's expect_tx; bytes from row and column
+      ptx::mbar_init(&empty[s], G + kTsC - 1);          // one commit from each CTA of the row and the column
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+    ptx::tma_prefetch_desc(a_blk ? &amaps.box[0] : &tmap_w);
+    ptx::tma_prefetch_desc(&tmap_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync_all();                              // barriers of the cluster initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0 && oblk < n_wblk) {       // W rows do not depend on earlier kernels
+    for (int kb = g; kb < min(num_kb, stages); kb += G) ptx::tma_prefetch_l2_2d(&tmap_w, kb * BK, o0);
+  }
+  ptx::grid_dependency_wait();                          // earlier kernels' writes are visible
+  ptx::grid_dependents_launch();                        // the next kernel may start its set-up
+  const int n_act = sh.n_ablk > 0 ? *sh.n_act : 0;
+  int my_box = 0;
+  const int my_rows = skinny_block_rows(oblk, n_oblk, n_wblk, sh, n_act, &my_box);
+  bool any_rows = false;                                // uniform across the cluster
+  for (int cc = 0; cc < kTsC; ++cc) {
+    int nb = 0;
+    any_rows |= skinny_block_rows(cl * kTsC + cc, n_oblk, n_wblk, sh, n_act, &nb) > 0;
+  }
+  const int n_exp_items = sh.n_dchunk ? (sh.meta.J == 1 ? sh.meta.counts[2] : sh.meta.T) * sh.n_dchunk : 0;
+
+  if (!any_rows) {
+    // nothing to multiply in this cluster
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // the block's A rows: one W box of 32 rows each, or one box per run of 2^k active slots with
+      // consecutive ids (largest power of two first); this CTA issues every G-th of them
+      int chunk_row[BM / 8], chunk_pos[BM / 8], chunk_k[BM / 8];
+      int n_chunk = 0;
+      if (a_blk) {
+        for (int i = 0; i < my_box;) {
+          const int s0 = sh.act_slot[a0 + i];
+          int run = 1;
+          while (i + run < my_box && sh.act_slot[a0 + i + run] == s0 + run) ++run;
+          const int k = 31 - __clz(run);                // 2^k <= run
+          chunk_row[n_chunk] = s0 * sh.R;
+          chunk_pos[n_chunk] = i;
+          chunk_k[n_chunk] = k;
+          ++n_chunk;
+          i += 1 << k;
+        }
+      }
+      const int a_bytes = oblk >= n_oblk ? 0 : (a_blk ? my_box * sh.R * BK * 2 : kSkinnyABytes);
+      // every CTA of a column receives a whole box of n_gmax x rows (past NT: zero fill)
+      const uint32_t bytes = static_cast<uint32_t>(a_bytes + n_gmax * BK * 2);
+      auto prefetch_rows = [&](int kbp) {               // the block's A rows of K block kbp into L2
+        if (a_blk) {
+          for (int i = 0; i < n_chunk; ++i) ptx::tma_prefetch_l2_2d(&amaps.box[chunk_k[i]], kbp * BK, chunk_row[i]);
+        } else if (oblk < n_oblk) {
+          ptx::tma_prefetch_l2_2d(&tmap_w, kbp * BK, o0);
+        }
+      };
+      int pf_next = stages + g;                         // next K block this CTA asks L2 for (step G)
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!ptx::mbar_wait_short(&empty[stage], phase ^ 1u, err)) break;
+        uint8_t* sa = smem + stage * stage_bytes;
+        ptx::mbar_arrive_expect_tx(&full[stage], bytes);
+        if (kb % G == g) {
+          if (a_blk) {
+            for (int i = 0; i < n_chunk; ++i)
+              ts_load(sa + chunk_pos[i] * sh.R * BK * 2, &amaps.box[chunk_k[i]], &full[stage], kb * BK, chunk_row[i],
+                      row_mask, self_bit);
+          } else if (oblk < n_oblk) {
+            ts_load(sa, &tmap_w, &full[stage], kb * BK, o0, row_mask, self_bit);
+          }
+        }
+        if (kb % kTsC == c) ts_load(sa + kSkinnyABytes, &tmap_x, &full[stage], kb * BK, t_g, col_mask, self_bit);
+        // at most one L2 request per K block, so that the copies the MMAs wait for go first
+        if (pf_next < num_kb && pf_next < kb + kTsPrefetchAhead) {
+          prefetch_rows(pf_next);
+          pf_next += G;
+        }
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
+      }
+      // tail: every commit addressed to this CTA's stage barriers has landed before it may exit
+      for (int i = 0; i < stages; ++i) {
+        if (!ptx::mbar_wait_short(&empty[stage], phase ^ 1u, err)) break;
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const bool compute = my_rows > 0;
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, n_g);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool mma_ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!ptx::mbar_wait_short(&full[stage], phase, err)) { mma_ok = false; break; }
+        ptx::tc_fence_after();
+        if (compute) {
+          const uint32_t a_addr = ptx::smem_u32(smem + stage * stage_bytes);
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(a_addr);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(a_addr + kSkinnyABytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            ptx::umma_bf16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        ptx::umma_commit_mc(&empty[stage], peer_mask);
+        if (++stage == stages) { stage = 0; phase ^= 1u; }
+      }
+      if (mma_ok) ptx::umma_commit(acc_full);
+    }
+  } else {
+    // While the main loop runs, bring into L2 the B rows the expand kernel will read (a share
+    // of its items per block).
+    for (int item = blockIdx.x; item < n_exp_items; item += gridDim.x)
+      expand_vfull_prefetch(sh.pool, sh.meta, item, sh.n_dchunk, threadIdx.x - 64, kGemmThreads - 64);
+    // TMEM lane = output row o of the block (warp w reads lanes 32*(w%4)..), columns = the group's
+    // tokens; each store instruction writes 32 consecutive outputs of one token
+    if (my_rows > 0 && ptx::mbar_wait_short(acc_full, 0, err)) {
+      ptx::tc_fence_after();
+      const int quarter = warp & 3;
+      const int o = quarter * 32 + lane;
+      float* out = a_blk ? sh.vfull + a0 * sh.R : y + o0;
+      const long ld = a_blk ? sh.vfull_ld : D;
+      const int cols = a_blk ? my_rows : min(BM, D - o0);
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int t_end = min(n_g, T - t_g);              // the group's real tokens
+#pragma unroll 1
+      for (int c0 = 0; c0 < n_g; c0 += 64) {           // two loads in flight per wait
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0), r0);
+        if (c0 + 32 < n_g) ptx::tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0 + 32), r1);
+        ptx::tmem_ld_wait();
+        if (o < cols) {
+          float* dst = out + static_cast<size_t>(t_g) * ld + o;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c0 + i < t_end) dst[static_cast<size_t>(c0 + i) * ld] = __uint_as_float(r0[i]);
+          if (c0 + 32 < n_g) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + 32 + i < t_end) dst[static_cast<size_t>(c0 + 32 + i) * ld] = __uint_as_float(r1[i]);
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync_all();                              // no CTA leaves while a peer may still address it
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -648,8 +888,77 @@ cudaError_t launch_skinny_pair(const uint16_t* x, const uint16_t* W, float* y, i
   return e;
 }
 
+// Token groups of the token-split form for this shape (0: its grid does not fit one wave): the
+// most groups (at most kTsMaxG, each of 16 tokens or more) whose grid fits one wave.
+int skinny_ts_groups(int NT, int n_oblk, int num_sms) {
+  const int n_cl = (n_oblk + kTsC - 1) / kTsC;
+  int G = 0;
+  for (int g = 1; g <= kTsMaxG && g <= NT / 16; ++g) {
+    const int real = (NT + ts_group_max(NT, g) - 1) / ts_group_max(NT, g);   // groups that hold tokens
+    if (real == g && n_cl * kTsC * g <= num_sms) G = g;
+  }
+  return G;
+}
+
+cudaError_t launch_skinny_ts(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
+                             int G, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
+  const int NT = (T + 15) / 16 * 16;
+  const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
+  const int n_cl = (n_oblk + kTsC - 1) / kTsC;
+  const int n_gmax = ts_group_max(NT, G);
+  const int stages = ts_stages(n_gmax);
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(n_gmax)) tmem_cols <<= 1;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_skinny_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTsSmemMax);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  CUtensorMap mw, mx;
+  SkinnyAMaps ma;
+  if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mx, x, T, K, n_gmax, BK))
+    return cudaErrorInvalidValue;
+  for (int k = 0; k < kABoxMaps; ++k) {
+    if (sh.n_ablk > 0 && (sh.R << k) <= BM) {
+      if (!make_tmap_bf16_impl(&ma.box[k], A_pool, static_cast<long>(S) * sh.R, K, sh.R << k, BK))
+        return cudaErrorInvalidValue;
+    } else {
+      ma.box[k] = mw;                                   // never used
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_cl * kTsC * G, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = ts_smem_bytes(n_gmax);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTsC * G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  note_launch_begin(kKindGemm, s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_skinny_ts_kernel, mw, mx, ma, y, T, D, K, NT, G, n_oblk, stages,
+                                     tmem_cols, err, sh);
+  note_launch_end(kKindGemm, s);
+  return e;
+}
+
 cudaError_t launch_skinny(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                           int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
+  const int NT = (T + 15) / 16 * 16;
+  // The split-K form unless the token-split one is asked for: the token-split form delivers each
+  // A row to all G CTAs of a row, and per-SM L2-to-SM bandwidth (about 100-115 GB/s measured in
+  // both forms) then bounds it well below the split-K form on the decode and compose shapes.
+  const int G = skinny_form() == 2 ? skinny_ts_groups(NT, (D + BM - 1) / BM + sh.n_ablk, num_sms) : 0;
+  if (G > 0) return launch_skinny_ts(x, W, y, T, K, D, err, G, A_pool, S, sh, s);
   return launch_skinny_pair(x, W, y, T, K, D, err, num_sms, A_pool, S, sh, s);
 }
 

@@ -158,6 +158,8 @@ cudaError_t launch_wait_check(uint32_t* err, cudaStream_t s);
 // launch_pair_gemm picks it. gemm_tile_n() is the process-wide choice set by
 // mlora_set_gemm_tile_n (0 automatic, -1 never the pair kernel, else that N tile).
 int pair_gemm_max_pairs();
+// Form of the small-batch GEMM set by mlora_set_skinny_form (0 and 1 split-K, 2 token-split).
+int skinny_form();
 // Whether launch_base_gemm_lora takes the CTA-pair kernel for a batch of T tokens, and whether
 // that kernel then also computes the shrink of the tensor-core side path (as tiles of its own
 // schedule) for inputs of width K.

@@ -51,6 +51,7 @@ mlora_status cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_gemm_tile_n{0};          // mlora_set_gemm_tile_n
+std::atomic<int> g_skinny_form{0};          // mlora_set_skinny_form
 std::atomic<int> g_path{0};                 // mlora_set_path
 
 // ---------------------------------------------------------------- trace
@@ -148,6 +149,7 @@ namespace mlora {
 int report_error(int status, const char* message) { return fail(status, "%s", message); }
 int report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 int gemm_tile_n() { return g_gemm_tile_n.load(std::memory_order_relaxed); }
+int skinny_form() { return g_skinny_form.load(std::memory_order_relaxed); }
 
 void note_launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -289,6 +291,12 @@ mlora_status mlora_set_gemm_tile_n(int n) {
   if (n != 0 && n != -1 && n != 256 && n != 224 && n != 192 && n != 128)
     return fail(MLORA_ERR_INVALID_ARG, "tile N must be 0 (automatic), -1 (one-CTA kernel), 256, 224, 192 or 128");
   g_gemm_tile_n.store(n);
+  return MLORA_OK;
+}
+
+mlora_status mlora_set_skinny_form(int form) {
+  if (form < 0 || form > 2) return fail(MLORA_ERR_INVALID_ARG, "form must be 0 (default, split-K), 1 (split-K) or 2 (token-split)");
+  g_skinny_form.store(form);
   return MLORA_OK;
 }
 

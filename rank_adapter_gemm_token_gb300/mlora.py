@@ -36,7 +36,7 @@ EXPORTS = (
     "mlora_meta_status", "mlora_meta_read", "mlora_linear", "mlora_base_gemm", "mlora_lora_shrink",
     "mlora_lora_expand", "mlora_status_string", "mlora_last_error", "mlora_version", "mlora_launch_count",
     "mlora_trace_enable", "mlora_trace_disable", "mlora_trace_read", "mlora_kernel_kind_name",
-    "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n", "mlora_check_wait_timeout",
+    "mlora_lora_apply_noalloc", "mlora_set_gemm_tile_n", "mlora_set_skinny_form", "mlora_check_wait_timeout",
     "mlora_load_adapter_sliced", "mlora_slot_cache_create", "mlora_slot_cache_destroy", "mlora_slot_cache_assign",
     "mlora_slot_cache_lookup", "mlora_slot_cache_pin", "mlora_slot_cache_evict", "mlora_adapter_cache_create",
     "mlora_adapter_cache_destroy", "mlora_adapter_cache_register", "mlora_adapter_cache_unregister",
@@ -96,6 +96,7 @@ def load(path: str | None = None):
             "mlora_trace_read": [i32, vp, vp],
             "mlora_lora_apply_noalloc": [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp],
             "mlora_set_gemm_tile_n": [i32],
+            "mlora_set_skinny_form": [i32],
             "mlora_check_wait_timeout": [vp],
             "mlora_load_adapter_sliced": [vp, i32, i32, vp, vp, vp, i32, f32, i32],
             "mlora_slot_cache_create": [i32, vp],
@@ -315,6 +316,11 @@ def mlora_set_path(path: int) -> None:
 def mlora_set_gemm_tile_n(n: int) -> None:
     """0 automatic, -1 never the CTA-pair GEMM, 256/224/192/128 always it with that N tile."""
     _check(load().mlora_set_gemm_tile_n(n), "mlora_set_gemm_tile_n")
+
+
+def mlora_set_skinny_form(form: int) -> None:
+    """Small-batch GEMM form: 0 and 1 split-K (CTA pairs), 2 token-split whenever it fits one wave."""
+    _check(load().mlora_set_skinny_form(form), "mlora_set_skinny_form")
 
 
 # ------------------------------------------------------------------------- slot residency

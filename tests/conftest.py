@@ -32,3 +32,11 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture
+def skinny_form():
+    """Sets the small-batch GEMM form for one test (mlora_set_skinny_form), automatic afterwards."""
+    from rank_adapter_gemm_token_gb300 import mlora
+    yield mlora.mlora_set_skinny_form
+    mlora.mlora_set_skinny_form(0)

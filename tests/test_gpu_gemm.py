@@ -66,6 +66,22 @@ def test_large_shapes_sampled(cuda_device, T, K, D):
     assert_close(y[rows], ref, f"gemm {T}x{K}x{D}")
 
 
+@pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("T,K,D", [(1, 64, 520), (17, 328, 4100), (250, 200, 2056), (64, 1032, 4096),
+                                   (256, 4096, 4096)])
+def test_small_batch_gemm_forms(cuda_device, skinny_form, form, T, K, D):
+    # both forms of the small-batch GEMM (split-K CTA pairs; token groups sharing W and x rows by
+    # multicast) on ragged token counts and a partial last output block; deterministic
+    from rank_adapter_gemm_token_gb300 import layer
+    skinny_form(form)
+    x, W, y = _run(T, K, D, seed=T + D + form)
+    rows = None if T * D <= 600_000 else np.unique(np.r_[0, T - 1, np.random.default_rng(1).integers(0, T, 30)])
+    ref = oracle.linear(x, W, np.full((T, 1), -1), {}, 1, rows=rows)
+    assert_close(y if rows is None else y[rows], ref, f"gemm {T}x{K}x{D} form {form}")
+    xd, Wd = layer.bf16_from_bits(x, "cuda"), layer.bf16_from_bits(W, "cuda")
+    assert np.array_equal(layer.base_gemm(xd, Wd).cpu().numpy(), y), "GEMM result differs between launches"
+
+
 @pytest.mark.parametrize("T,K,D", [(200, 320, 136), (1900, 200, 2600)])
 def test_small_integers_are_exact(cuda_device, T, K, D):
     # Small integers in bf16 give exact fp32 products and sums: the GPU must equal the oracle bit

@@ -140,6 +140,44 @@ def test_decode_shapes_on_both_paths(cuda_device, path):
         mlora.mlora_set_path(0)
 
 
+@pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("T,K,D,S,R,J,seed", [(250, 200, 4100, 30, 16, 1, 80), (33, 264, 600, 9, 32, 2, 81),
+                                              (1, 72, 136, 3, 8, 1, 82), (176, 512, 1000, 12, 64, 3, 83),
+                                              (256, 4096, 4096, 100, 16, 1, 84)])
+def test_small_batch_gemm_forms(cuda_device, skinny_form, form, T, K, D, S, R, J, seed):
+    """The small-batch path with each form of its GEMM (1: split-K CTA pairs; 2: token groups with
+    W and x rows shared by multicast) and the shrink folded in: ragged token counts (groups with
+    padding rows), a partial last output block, several slots per token, rank up to R; against
+    the oracle, and bit-identical over repeated steps."""
+    from rank_adapter_gemm_token_gb300 import mlora
+    skinny_form(form)
+    rng = np.random.default_rng(seed)
+    lin = synth.Linear("lin", K, D, synth.normal_bf16(seed, 10, (D, K), 0.02), 0)
+    for s in range(S):
+        r = int(rng.integers(1, R + 1))
+        lin.adapters[s] = synth.Adapter(A=synth.normal_bf16(seed, 100 + s, (r, K), 0.02),
+                                        B=synth.normal_bf16(seed, 300 + s, (D, r), 0.02),
+                                        rank=r, alpha=float(rng.integers(1, 3 * r)), rslora=bool(s % 3 == 0))
+    slots = rng.integers(-1, S, size=(T, J)).astype(np.int32)
+    slots[::7, :] = -1
+    scales = rng.uniform(0.2, 1.0, size=(T, J)).astype(np.float32)
+    wl = synth.Workload("forms", seed, T, J, S, R, slots, scales, {0: synth.normal_bf16(seed, 11, (T, K), 1.0)}, [lin])
+    mlora.mlora_set_path(1)
+    try:
+        dw = DeviceWorkload(wl)
+        dw.run()
+        dw.meta.status()
+        first = dw.linears[0].y.cpu().numpy()
+        dw.run()
+        dw.meta.status()
+        assert np.array_equal(dw.linears[0].y.cpu().numpy(), first), "the small-batch path is not deterministic"
+        rows = None if T * D <= 300_000 else sample_rows(wl, 40)
+        _check_linear(wl, dw, dw.linears[0], rows=rows)
+        dw.close()
+    finally:
+        mlora.mlora_set_path(0)
+
+
 def test_compose_config_full_size(cuda_device):
     wl = synth.compose()
     dw = DeviceWorkload(wl)
