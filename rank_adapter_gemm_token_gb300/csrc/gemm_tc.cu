@@ -308,7 +308,7 @@ __device__ __forceinline__ void skinny_pull(cooperative_groups::cluster_group& c
 // that read both CTAs' operands, accumulating each block in its own CTA's TMEM. Per 64-wide K
 // block an SM then stages 16 KB of A rows and 16 KB of x instead of 16 + 32 KB, so six stages fit
 // where four did, and x is read from L2 half as often. The K shares of a block (ranks h, h + 2,
-// ...) reduce their partials as in the one-CTA form. A pair whose even block has no rows (an A
+// ...) reduce their partials with skinny_pull (above). A pair whose even block has no rows (an A
 // block past the active slots, or a block past the grid) skips the main loop; an odd block
 // without rows still stages its half of x and lets the pair compute rows that are then dropped.
 constexpr int kSkinnyPairStages = 6;

@@ -85,7 +85,7 @@ def test_small_batch_gemm_forms(cuda_device, skinny_form, form, T, K, D):
 @pytest.mark.parametrize("T,K,D", [(200, 320, 136), (1900, 200, 2600)])
 def test_small_integers_are_exact(cuda_device, T, K, D):
     # Small integers in bf16 give exact fp32 products and sums: the GPU must equal the oracle bit
-    # for bit (one-CTA skinny kernel; CTA-pair kernel with a ragged last pair tile).
+    # for bit (small-batch CTA-pair kernel; large-batch CTA-pair kernel with a ragged last pair tile).
     from rank_adapter_gemm_token_gb300 import layer
     rng = np.random.default_rng(5)
     xf = rng.integers(-3, 4, size=(T, K)).astype(np.float32)
