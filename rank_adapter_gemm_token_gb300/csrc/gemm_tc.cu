@@ -833,6 +833,43 @@ cudaError_t launch_tc(const uint16_t* x, const uint16_t* W, float* y, int T, int
 }
 
 
+// Clusters of 2 x splitk CTAs of the CTA-pair small-batch kernel (one per SM: its shared memory)
+// that can be resident at once on this device, cached per device and split. A cluster is placed
+// within one GPC, so the count is not the SM count over the cluster size: GB300 reports 76, 36,
+// 23 and 15 for splits 1-4, and a launch one cluster past that (24 clusters of 6, 16 of 8) took
+// 34-35 us where the next smaller split took 23-25 us.
+int skinny_pair_resident_clusters(int splitk) {
+  static int cached_device = -1;
+  static int cached[kSkinnyPairMaxSplit + 1] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cached_device != dev) {
+    int num_sms = 0;
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int k = 1; k <= kSkinnyPairMaxSplit; ++k) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(num_sms / (2 * k) * (2 * k), 1, 1);
+      cfg.blockDim = dim3(kGemmThreads, 1, 1);
+      cfg.dynamicSmemBytes = skinny_pair_smem_bytes(256);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2 * k;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, gemm_bf16_skinny_pair_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        clusters = num_sms / (2 * k);                   // the count by SMs alone
+      }
+      cached[k] = clusters;
+    }
+    cached_device = dev;
+  }
+  return cached[splitk];
+}
+
 // The CTA-pair form: pairs of output blocks, K split over clusters of 2 x splitk CTAs.
 cudaError_t launch_skinny_pair(const uint16_t* x, const uint16_t* W, float* y, int T, int K, int D, uint32_t* err,
                                int num_sms, const uint16_t* A_pool, int S, const SkinnyShrink& sh, cudaStream_t s) {
@@ -840,12 +877,6 @@ cudaError_t launch_skinny_pair(const uint16_t* x, const uint16_t* W, float* y, i
   const int n_oblk = (D + BM - 1) / BM + sh.n_ablk;
   const int n_pairs = (n_oblk + 1) / 2;
   const int num_kb = (K + BK - 1) / BK;
-  int splitk = num_sms / (2 * n_pairs);
-  if (splitk > kSkinnyPairMaxSplit) splitk = kSkinnyPairMaxSplit;
-  if (splitk > num_kb) splitk = num_kb;
-  if (splitk < 1) splitk = 1;
-  uint32_t tmem_cols = 32;
-  while (tmem_cols < static_cast<uint32_t>(NT)) tmem_cols <<= 1;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -855,6 +886,15 @@ cudaError_t launch_skinny_pair(const uint16_t* x, const uint16_t* W, float* y, i
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  // the widest K split whose clusters are all resident at once (a second wave of clusters costs
+  // more than the shorter main loop saves)
+  int splitk = num_sms / (2 * n_pairs);
+  if (splitk > kSkinnyPairMaxSplit) splitk = kSkinnyPairMaxSplit;
+  if (splitk > num_kb) splitk = num_kb;
+  if (splitk < 1) splitk = 1;
+  while (splitk > 1 && n_pairs > skinny_pair_resident_clusters(splitk)) --splitk;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(NT)) tmem_cols <<= 1;
   CUtensorMap mw, mxh;
   SkinnyAMaps ma;
   if (!make_tmap_bf16_impl(&mw, W, D, K, BM, BK) || !make_tmap_bf16_impl(&mxh, x, T, K, NT / 2, BK))
