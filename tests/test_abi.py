@@ -108,3 +108,14 @@ def test_gemm_tile_choice_is_validated(lib):
     for n in (1, 64, 160, 512, -2):
         assert lib.mlora_set_gemm_tile_n(n) == mlora.MLORA_ERR_INVALID_ARG
     assert lib.mlora_set_gemm_tile_n(0) == mlora.MLORA_OK
+
+
+def test_path_and_small_batch_form_choices_are_validated(lib):
+    from rank_adapter_gemm_token_gb300 import mlora
+    for setter, good, bad in ((lib.mlora_set_path, (0, 1, 2), (-1, 3)),
+                              (lib.mlora_set_skinny_form, (0, 1, 2), (-1, 3, 7))):
+        for v in good:
+            assert setter(v) == mlora.MLORA_OK
+        for v in bad:
+            assert setter(v) == mlora.MLORA_ERR_INVALID_ARG
+        assert setter(0) == mlora.MLORA_OK
