@@ -96,3 +96,16 @@ def test_phase_rows_cover_the_mixed_step():
     assert plan.phases[0][2] == plan.phases[1][1] == 768
     sub = bench.sub_workload(plan, 768, plan.T)
     assert sub.T == 256 and sub.token_slots.shape == (256, 1)
+
+
+def test_tensor_peak_follows_the_power_cap():
+    # the sustained bf16 figure only when the power cap throttled the timed steps; HBM unchanged
+    peaks = {"hbm_gbs": 6698.2, "bf16_tflops": 1883.1, "bf16_tflops_sustained": 1710.1}
+    capped, note = bench.tensor_peak_for(peaks, "measured", {"reasons": ["sw_power_cap"]})
+    assert capped["bf16_tflops"] == 1710.1 and capped["hbm_gbs"] == 6698.2 and "sustained" in note
+    for clocks in ({"reasons": []}, {"reasons": ["hw_slowdown"]}, None, {}):
+        free, note = bench.tensor_peak_for(peaks, "measured", clocks)
+        assert free["bf16_tflops"] == 1883.1 and "burst" in note
+    assert peaks["bf16_tflops"] == 1883.1                       # the caller's dict is left alone
+    rf = bench.roofline_of(1e6, 1.7e12, 1e-3, capped)           # 1.7 PFLOP/s of work for 1 ms
+    assert rf["bound"] == "tensor" and abs(rf["frac"] - 1700.0 / 1710.1) < 1e-9
